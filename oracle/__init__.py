@@ -1,0 +1,152 @@
+"""fp64 CPU oracle for the attention forward -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg may import this package.  It shares no code with the CUDA path
+(``scaled_dot_product_18_b300``) and never imports it; the two meet only in the
+tests' comparisons, on inputs drawn by the seeded generator.
+
+Two independent implementations of the same definition:
+
+* ``attention_rows`` -- plain C (``attn_oracle.c``), float64, one query row at a
+  time with a two-pass max-shifted softmax, threaded over rows.  Used for
+  parity at every size (on sampled rows at the large ones) and as the timed
+  CPU baseline.
+* ``attention_literal`` -- numpy float64, materialises the full score matrix,
+  applies the mask by filling with -inf, takes the softmax along the key axis
+  and multiplies by V, in the order the pages' reference snippets write it
+  (hotelren.com "AI attention: essence and evolution", ch.1 code and sec. 2.1;
+  qqiyuan.cn "Multi-head attention in the Transformer: implementation and
+  performance", baseline implementation).  Tiny inputs only.
+
+Every function is pinned by ``tests/test_oracle.py`` against closed forms,
+invariants and hand-derived fixtures (``tests/golden/``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "attn_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle with gcc (no fast-math: sums stay in key order)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp.%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-pthread", "-std=c11",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        f = lib.oracle_attn_fwd
+        dp = ctypes.POINTER(ctypes.c_double)
+        f.argtypes = [dp, dp, dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                      ctypes.c_double, ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                      ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, dp, dp, ctypes.c_int]
+        f.restype = ctypes.c_int
+        _lib = lib
+    return _lib
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact decode of bfloat16 bit patterns (uint16) to float64."""
+    u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return u.view(np.float32).astype(np.float64)
+
+
+def _as_f64(x: np.ndarray) -> np.ndarray:
+    x = np.asarray(x)
+    if x.dtype == np.uint16:
+        x = bf16_to_f64(x)
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+def attention_rows(q, k, v, scale: float, causal: bool, key_lens=None, rows=None,
+                   threads: int | None = None):
+    """Row-mode oracle.  q: [B, H, Nq, d]; k, v: [B, H, Nk, d] (float64, or
+    uint16 bf16 bits).  Query and key positions share one axis from 0, so the
+    causal rule is j <= i; self-attention has Nq == Nk.
+
+    key_lens: int [B] or None (all keys visible).  rows: query indices to
+    compute (the same for every (b, h)) or None for all.  Returns
+    ``(O, lse)`` as float64 arrays [B, H, R, d] and [B, H, R].
+    """
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    assert k.shape == (B, H, Nk, d) and v.shape == k.shape
+    if rows is None:
+        rows_arr, n_rows = None, Nq
+    else:
+        rows_arr = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        n_rows = rows_arr.size
+    out = np.zeros((B, H, n_rows, d), dtype=np.float64)
+    lse = np.zeros((B, H, n_rows), dtype=np.float64)
+    kl = None
+    if key_lens is not None:
+        kl = np.ascontiguousarray(np.asarray(key_lens, dtype=np.int32))
+        assert kl.shape == (B,)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib = _load()
+    rc = lib.oracle_attn_fwd(
+        q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp), B, H, Nq, Nk, d,
+        float(scale), int(bool(causal)),
+        kl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if kl is not None else None,
+        rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if rows_arr is not None else None,
+        n_rows, out.ctypes.data_as(dp), lse.ctypes.data_as(dp),
+        int(threads or default_threads()))
+    if rc != 0:
+        raise ValueError("oracle_attn_fwd rejected its arguments (rc=%d)" % rc)
+    return out, lse
+
+
+def visible_mask(N: int, causal: bool, key_len: int | None) -> np.ndarray:
+    """[N, N] boolean: key j visible to query i (j < key_len, and j <= i if causal)."""
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    keep = np.ones((N, N), dtype=bool)
+    if key_len is not None:
+        keep &= j < key_len
+    if causal:
+        keep &= j <= i
+    return keep
+
+
+def attention_literal(q, k, v, scale: float, causal: bool, key_lens=None):
+    """Materialised-matrix oracle: returns ``(O, lse, P)``, all float64.
+
+    S = scale * Q K^T; S[~visible] = -inf; P = softmax(S) along keys; O = P V;
+    lse = max + ln(sum exp(S - max)).  A row with no visible key gets P = 0,
+    O = 0 and lse = -inf (instead of the NaN a literal -inf fill would give).
+    """
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, N, d = q.shape
+    S = scale * np.matmul(q, np.swapaxes(k, -1, -2))  # [B, H, N, N]
+    keep = np.stack([visible_mask(N, causal, None if key_lens is None else int(key_lens[b]))
+                     for b in range(B)])[:, None]  # [B, 1, N, N]
+    S = np.where(keep, S, -np.inf)
+    m = S.max(axis=-1, keepdims=True)
+    empty = ~np.isfinite(m)
+    m_safe = np.where(empty, 0.0, m)
+    E = np.where(keep, np.exp(S - m_safe), 0.0)
+    l = E.sum(axis=-1, keepdims=True)
+    P = np.where(empty, 0.0, E / np.where(empty, 1.0, l))
+    O = np.matmul(P, v)
+    with np.errstate(divide="ignore"):
+        lse = np.where(empty, -np.inf, m_safe + np.log(np.where(empty, 1.0, l)))[..., 0]
+    return O, lse, P

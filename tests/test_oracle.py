@@ -1,0 +1,292 @@
+"""Pins for the fp64 oracle, independent of the oracle's own code.
+
+Each test checks the oracle against something the pages or the mathematics
+fix -- hand-derived closed forms (tests/golden), invariants and special cases
+of masked softmax attention -- chosen so that a dropped term, a wrong sign or
+index, a transposed operand, a wrong log base or an off-by-one in a mask fails
+at least one of them (see test_pins_catch_planted_mistakes).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "two_key_closed_form.json")
+MODES = ["rows", "literal"]
+
+
+def run(mode, q, k, v, scale, causal, key_lens=None):
+    if mode == "rows":
+        return oracle.attention_rows(q, k, v, scale, causal, key_lens, threads=2)
+    O, lse, _ = oracle.attention_literal(q, k, v, scale, causal, key_lens)
+    return O, lse
+
+
+def rnd(seed, B, H, N, d, scale=1.0):
+    r = np.random.default_rng(seed)
+    return [scale * r.standard_normal((B, H, N, d)) for _ in range(3)]
+
+
+# --- hand-derived closed forms -------------------------------------------------
+
+@pytest.mark.parametrize("mode", MODES)
+def test_golden_closed_forms(mode):
+    cases = json.load(open(GOLDEN))["cases"]
+    for c in cases:
+        q = np.array(c["q"])[None, None]
+        k = np.array(c["k"])[None, None]
+        v = np.array(c["v"])[None, None]
+        kl = None if c["key_len"] is None else np.array([c["key_len"]], dtype=np.int32)
+        O, lse = run(mode, q, k, v, c["scale"], c["causal"], kl)
+        np.testing.assert_allclose(O[0, 0], np.array(c["O"]), rtol=0, atol=1e-12, err_msg=c["name"])
+        np.testing.assert_allclose(lse[0, 0], np.array(c["lse"]), rtol=0, atol=1e-12, err_msg=c["name"])
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_textbook_two_term_softmax(mode):
+    # d = 1, N = 2: softmax of two logits is the logistic function of their
+    # difference, O = v0 + (v1 - v0) * sigma(s1 - s0).
+    r = np.random.default_rng(5)
+    for _ in range(20):
+        q, k, v = r.standard_normal((3, 1, 1, 2, 1))
+        scale = r.uniform(0.1, 2.0)
+        O, lse = run(mode, q, k, v, scale, False)
+        for i in range(2):
+            s0, s1 = scale * q[0, 0, i, 0] * k[0, 0, 0, 0], scale * q[0, 0, i, 0] * k[0, 0, 1, 0]
+            sig = 1.0 / (1.0 + math.exp(-(s1 - s0)))
+            want = v[0, 0, 0, 0] + (v[0, 0, 1, 0] - v[0, 0, 0, 0]) * sig
+            assert abs(O[0, 0, i, 0] - want) < 1e-12
+            assert abs(lse[0, 0, i] - (max(s0, s1) + math.log1p(math.exp(-abs(s1 - s0))))) < 1e-12
+
+
+# --- invariants and special cases ---------------------------------------------
+
+def test_literal_rows_sum_to_one():
+    q, k, v = rnd(1, 2, 2, 19, 4)
+    for causal in (False, True):
+        for kl in (None, np.array([3, 19], dtype=np.int32)):
+            _, _, P = oracle.attention_literal(q, k, v, 0.5, causal, kl)
+            np.testing.assert_allclose(P.sum(-1), 1.0, atol=1e-12)
+            assert (P >= 0).all()
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_constant_v_gives_that_row(mode):
+    q, k, _ = rnd(2, 2, 3, 23, 6, scale=2.0)
+    c = np.random.default_rng(3).standard_normal(6)
+    v = np.broadcast_to(c, q.shape).copy()
+    for causal in (False, True):
+        O, _ = run(mode, q, k, v, 0.7, causal, np.array([1, 23], dtype=np.int32))
+        np.testing.assert_allclose(O, np.broadcast_to(c, O.shape), atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_zero_q_gives_mean_of_visible_v(mode):
+    _, k, v = rnd(4, 2, 2, 21, 5)
+    q = np.zeros_like(k)
+    kl = np.array([7, 21], dtype=np.int32)
+    O, lse = run(mode, q, k, v, 0.9, False, kl)
+    for b in range(2):
+        n = kl[b]
+        np.testing.assert_allclose(O[b], np.broadcast_to(v[b, :, :n].mean(axis=1, keepdims=True), O[b].shape),
+                                   atol=1e-12)
+        np.testing.assert_allclose(lse[b], math.log(n), atol=1e-12)
+    # causal: row i sees keys 0..i
+    O, lse = run(mode, q, k, v, 0.9, True, None)
+    for i in range(21):
+        np.testing.assert_allclose(O[:, :, i], v[:, :, : i + 1].mean(axis=2), atol=1e-12)
+        np.testing.assert_allclose(lse[:, :, i], math.log(i + 1), atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_causal_row0_is_v0(mode):
+    q, k, v = rnd(6, 2, 3, 17, 8)
+    O, lse = run(mode, q, k, v, 0.25, True)
+    np.testing.assert_allclose(O[:, :, 0], v[:, :, 0], atol=1e-12)
+    s00 = 0.25 * np.einsum("bhd,bhd->bh", q[:, :, 0], k[:, :, 0])
+    np.testing.assert_allclose(lse[:, :, 0], s00, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_single_visible_key(mode):
+    q, k, v = rnd(7, 3, 2, 13, 4, scale=3.0)
+    kl = np.ones(3, dtype=np.int32)
+    for causal in (False, True):
+        O, lse = run(mode, q, k, v, 1.0, causal, kl)
+        np.testing.assert_allclose(O, np.broadcast_to(v[:, :, :1], O.shape), atol=1e-12)
+        s = np.einsum("bhid,bhd->bhi", q, k[:, :, 0])
+        np.testing.assert_allclose(lse, s, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_no_visible_key_gives_zero_and_minus_inf(mode):
+    q, k, v = rnd(8, 2, 1, 9, 4)
+    O, lse = run(mode, q, k, v, 1.0, False, np.array([0, 9], dtype=np.int32))
+    assert np.all(O[0] == 0.0) and np.all(np.isneginf(lse[0]))
+    assert np.all(np.isfinite(O[1])) and np.all(np.isfinite(lse[1]))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_key_permutation_invariance(mode):
+    q, k, v = rnd(9, 1, 2, 31, 8)
+    perm = np.random.default_rng(10).permutation(31)
+    O1, l1 = run(mode, q, k, v, 0.4, False)
+    O2, l2 = run(mode, q, k[:, :, perm], v[:, :, perm], 0.4, False)
+    np.testing.assert_allclose(O1, O2, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_shift_invariance(mode):
+    # K -> K + 1 u^T shifts row i's logits by scale*(q_i . u): O is unchanged and
+    # lse moves by exactly that amount.
+    q, k, v = rnd(11, 2, 2, 25, 6)
+    u = np.random.default_rng(12).standard_normal(6) * 3.0
+    for causal in (False, True):
+        O1, l1 = run(mode, q, k, v, 0.6, causal)
+        O2, l2 = run(mode, q, k + u, v, 0.6, causal)
+        np.testing.assert_allclose(O1, O2, atol=1e-10)
+        np.testing.assert_allclose(l2 - l1, 0.6 * (q @ u), atol=1e-10)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_linearity_in_v(mode):
+    q, k, v1 = rnd(13, 2, 2, 18, 4)
+    v2 = np.random.default_rng(14).standard_normal(v1.shape)
+    for causal in (False, True):
+        a, _ = run(mode, q, k, v1, 0.5, causal)
+        b, _ = run(mode, q, k, v2, 0.5, causal)
+        c, _ = run(mode, q, k, v1 + v2, 0.5, causal)
+        np.testing.assert_allclose(a + b, c, atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_huge_logits_stay_finite(mode):
+    # Without the max shift exp(1000) overflows; with it the softmax becomes a
+    # hard argmax and O is the V row of the largest logit.
+    q = np.zeros((1, 1, 3, 2)); q[..., 0] = 1.0
+    k = np.zeros((1, 1, 3, 2)); k[0, 0, :, 0] = [1000.0, 1200.0, 900.0]
+    v = np.arange(6, dtype=np.float64).reshape(1, 1, 3, 2)
+    O, lse = run(mode, q, k, v, 1.0, False)
+    np.testing.assert_allclose(O[0, 0], np.broadcast_to(v[0, 0, 1], (3, 2)), atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], 1200.0, atol=1e-9)
+
+
+def test_chunked_lse_and_merge_identity():
+    # aicoding.csdn.net "Why attention stalls large-model training", sec. 2.2:
+    # lse(x) = M + ln sum_chunks exp(lse_chunk - M) for any chunking.  The same
+    # identity merges partial outputs: O = sum_c exp(lse_c - lse) O_c.
+    q, k, v = rnd(15, 1, 2, 40, 8, scale=1.5)
+    O, lse = oracle.attention_rows(q, k, v, 0.35, False)
+    bounds = [0, 7, 8, 23, 40]
+    Os, ls = [], []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        Oc, lc = oracle.attention_rows(q, np.ascontiguousarray(k[:, :, a:b]), v[:, :, a:b].copy(), 0.35, False,
+                                       rows=np.arange(40))
+        Os.append(Oc); ls.append(lc)
+    # the chunks are [a, b) key ranges computed on sub-sequences of length b - a;
+    # rows index the query positions of the full sequence
+    ls = np.stack(ls)
+    M = ls.max(axis=0)
+    lse_merged = M + np.log(np.exp(ls - M).sum(axis=0))
+    np.testing.assert_allclose(lse_merged, lse, atol=1e-12)
+    O_merged = sum(np.exp(lc - lse)[..., None] * Oc for lc, Oc in zip(ls, Os))
+    np.testing.assert_allclose(O_merged, O, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_rows_equal_literal_brute_force(causal):
+    for (B, H, N, d) in [(1, 1, 1, 1), (2, 3, 16, 8), (1, 2, 13, 3), (3, 1, 7, 5)]:
+        q, k, v = rnd(100 + N, B, H, N, d, scale=2.0)
+        kl = np.random.default_rng(N).integers(0, N + 1, size=B).astype(np.int32)
+        for key_lens in (None, kl):
+            O1, l1 = oracle.attention_rows(q, k, v, 0.45, causal, key_lens)
+            O2, l2, _ = oracle.attention_literal(q, k, v, 0.45, causal, key_lens)
+            np.testing.assert_allclose(O1, O2, atol=1e-12)
+            np.testing.assert_array_equal(np.isneginf(l1), np.isneginf(l2))
+            fin = np.isfinite(l2)
+            np.testing.assert_allclose(l1[fin], l2[fin], atol=1e-12)
+
+
+def test_row_subset_matches_full():
+    q, k, v = rnd(16, 2, 2, 33, 4)
+    O, l = oracle.attention_rows(q, k, v, 0.5, True, np.array([20, 33], dtype=np.int32))
+    rows = [0, 5, 19, 20, 32]
+    Os, ls = oracle.attention_rows(q, k, v, 0.5, True, np.array([20, 33], dtype=np.int32), rows=rows)
+    np.testing.assert_array_equal(Os, O[:, :, rows])
+    np.testing.assert_array_equal(ls, l[:, :, rows])
+
+
+def test_bf16_decode_is_exact():
+    bits = np.array([0x0000, 0x8000, 0x3F80, 0xBF80, 0x4049, 0x7F7F, 0x0001], dtype=np.uint16)
+    want = [0.0, -0.0, 1.0, -1.0, 3.140625, 3.3895313892515355e38, 2.0 ** -133]
+    np.testing.assert_array_equal(oracle.bf16_to_f64(bits), np.array(want))
+
+
+def test_bad_arguments_rejected():
+    q, k, v = rnd(17, 1, 1, 4, 2)
+    with pytest.raises(ValueError):
+        oracle.attention_rows(q, k, v, 1.0, False, rows=[0, 4])
+
+
+# --- the pins must catch plausible mistakes -------------------------------------
+
+def _mutant(kind):
+    """A copy of the literal definition with one planted mistake."""
+    def f(q, k, v, scale, causal, key_lens=None):
+        q, k, v = [np.asarray(x, dtype=np.float64) for x in (q, k, v)]
+        B, H, N, d = q.shape
+        sc = 1.0 if kind == "no_scale" else scale
+        S = sc * (np.matmul(k, np.swapaxes(q, -1, -2)) if kind == "transposed" else
+                  np.matmul(q, np.swapaxes(k, -1, -2)))
+        i = np.arange(N)[:, None]; j = np.arange(N)[None, :]
+        keep = np.ones((B, 1, N, N), dtype=bool)
+        for b in range(B):
+            if key_lens is not None:
+                kl = int(key_lens[b])
+                keep[b, 0] &= (i < kl) if kind == "mask_queries" else (j < kl)
+            if causal:
+                keep[b, 0] &= (j < i) if kind == "causal_strict" else (j <= i)
+        S = np.where(keep, S, -np.inf)
+        m = S.max(-1, keepdims=True)
+        m = np.where(np.isfinite(m), m, 0.0)
+        E = np.where(keep, np.exp(S - m), 0.0)
+        l = E.sum(-1, keepdims=True)
+        l = np.where(l > 0, l, 1.0)
+        P = E / (1.0 if kind == "no_normalise" else l)
+        O = np.matmul(P, v)
+        lse = (m + (np.log2(l) if kind == "log2_lse" else np.log(l)))[..., 0]
+        if kind == "lse_no_max":
+            lse = np.log(l)[..., 0]
+        return O, lse
+    return f
+
+
+def _all_pins_pass(fn):
+    """Re-run the value pins above against ``fn``; False as soon as one fails."""
+    checks = []
+    cases = json.load(open(GOLDEN))["cases"]
+    for c in cases:
+        q = np.array(c["q"])[None, None]; k = np.array(c["k"])[None, None]; v = np.array(c["v"])[None, None]
+        kl = None if c["key_len"] is None else np.array([c["key_len"]], dtype=np.int32)
+        O, lse = fn(q, k, v, c["scale"], c["causal"], kl)
+        checks.append(np.allclose(O[0, 0], c["O"], atol=1e-9) and np.allclose(lse[0, 0], c["lse"], atol=1e-9))
+    q, k, v = rnd(6, 1, 2, 9, 4)
+    O, lse = fn(q, k, v, 0.25, True)
+    checks.append(np.allclose(O[:, :, 0], v[:, :, 0], atol=1e-9))
+    qz = np.zeros_like(q)
+    O, lse = fn(qz, k, v, 0.9, False, np.array([4], dtype=np.int32))
+    checks.append(np.allclose(O[0], v[0, :, :4].mean(axis=1, keepdims=True), atol=1e-9)
+                  and np.allclose(lse, math.log(4), atol=1e-9))
+    return all(checks)
+
+
+@pytest.mark.parametrize("kind", ["no_scale", "transposed", "mask_queries", "causal_strict",
+                                  "no_normalise", "log2_lse", "lse_no_max"])
+def test_pins_catch_planted_mistakes(kind):
+    assert _all_pins_pass(_mutant("none"))
+    assert not _all_pins_pass(_mutant(kind)), kind
