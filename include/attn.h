@@ -1,0 +1,104 @@
+/*
+ * attn.h -- C ABI of the B300 (sm_103a) multi-head scaled dot-product
+ * attention forward.
+ *
+ * The operation (one call computes every batch b and head h):
+ *
+ *   O[b,h] = softmax(Q[b,h] K[b,h]^T * scale + mask) V[b,h]
+ *   lse[b,h,i] = ln sum_j exp(scale * q_i . k_j)     over the visible keys j
+ *
+ *   -- hotelren.com "AI attention: essence and evolution", sec. 2.1 (the
+ *      softmax-attention formula, scaled by 1/sqrt(d_k)) and ch.1 code (the
+ *      mask fills hidden scores with -inf before the softmax);
+ *   -- aicoding.csdn.net "Why attention stalls large-model training",
+ *      sec. 2.2 (max-shifted softmax and the log-sum-exp, natural log);
+ *   -- hotelren.com sec. 4.1 (FlashAttention-1: tiles of Q and K/V, online
+ *      softmax, the n x n score matrix is never written out).
+ *
+ * Mask: key j is visible to query i iff j < key_lens[b] (a key-padding mask,
+ * lshu.cn "Self-attention meets the compute wall", sec. 4.1 and 5.2) and,
+ * when causal != 0, j <= i (only earlier positions and the query itself;
+ * hotelren.com sec. 2.1 note 2).  A hidden key gets exactly zero weight.
+ * A query row with no visible key (only possible with key_lens[b] == 0)
+ * gets O = 0 and lse = -inf.
+ *
+ * Every call is asynchronous on `stream`; the library never allocates device
+ * memory and never synchronises inside attn_fwd.
+ */
+#ifndef SDP18_ATTN_H
+#define SDP18_ATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_EINVAL = -1,      /* bad argument: null pointer, negative size, index overflow, scale */
+    ATTN_EUNSUPPORTED = -2,/* head dimension d other than 64 or 128 */
+    ATTN_EALIGN = -3,      /* a tensor pointer not 16-byte aligned (TMA requirement) */
+    ATTN_ECUDA = -4,       /* CUDA runtime/driver error (launch, tensor-map encode, no sm_103a device) */
+    ATTN_EDEVICE = -5      /* the kernel reported an error (a bounded wait ran out) */
+} attn_status;
+
+/*
+ * attn_fwd -- attention forward for all B*H heads in one launch.
+ *
+ * q, k, v : device, bf16, [B, H, N, d], contiguous, d fastest (the
+ *           multi-head split layout (batch, heads, seq_len, head_dim) of
+ *           hotelren.com sec. 2.2).  Read only.
+ * out     : device, bf16, [B, H, N, d], contiguous.  Written: every row
+ *           0..N-1 of every head, fp32-accumulated and rounded to nearest
+ *           even.  Must not overlap q, k, v or lse.
+ * lse     : device, fp32, [B, H, N], or NULL (not written).  Natural-log
+ *           log-sum-exp of the scaled, masked logits of each query row.
+ * B, H, N : batch, heads, sequence length (queries = keys = N).  Negative
+ *           -> ATTN_EINVAL.  B*H*N == 0 -> ATTN_OK, nothing launched, no
+ *           pointer checked.  B*H and N must each be < 2^31 and the tile
+ *           grid ceil(N/128)*B*H must fit a 1-D grid, else ATTN_EINVAL.
+ * d       : head dimension, 64 or 128 (else ATTN_EUNSUPPORTED).
+ * scale   : multiplier of q.k, finite and > 0 (else ATTN_EINVAL); usually
+ *           1/sqrt(d).
+ * causal  : non-zero = query i sees keys j <= i only.
+ * key_lens: device, int32 [B], or NULL (all N keys visible).  The kernel
+ *           clamps each value to [0, N]; keys j >= key_lens[b] are hidden
+ *           for every head and every query of batch b.  Query rows are never
+ *           masked: all N rows are computed and written.
+ * stream  : CUDA stream the kernel is launched on.
+ *
+ * Ownership: every buffer belongs to the caller and must stay valid until
+ * the stream has finished the call.  Returns ATTN_OK once launched; errors
+ * found on the host are returned before anything is enqueued.  Device-side
+ * errors are reported by attn_check_device.
+ */
+attn_status attn_fwd(const void *q, const void *k, const void *v,
+                     void *out, float *lse,
+                     int B, int H, int N, int d, float scale, int causal,
+                     const int32_t *key_lens, attn_stream_t stream);
+
+/*
+ * attn_check_device -- synchronise `stream`, then read and clear the
+ * library's device error word on the current device.  Returns ATTN_EDEVICE
+ * if a kernel since the last check gave up on a bounded wait (its outputs are
+ * then incomplete), ATTN_ECUDA on a CUDA error, else ATTN_OK.
+ */
+attn_status attn_check_device(attn_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *attn_status_str(attn_status s);
+
+/* ABI version of this header (bumped on any signature change). */
+int attn_abi_version(void);
+
+#define ATTN_ABI_VERSION 1
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDP18_ATTN_H */

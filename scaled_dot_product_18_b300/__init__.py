@@ -1,1 +1,122 @@
-"""B300-native multi-head scaled dot-product attention forward (placeholder binding)."""
+"""B300-native multi-head scaled dot-product attention forward.
+
+Python binding of the C ABI in ``include/attn.h`` (library ``libattn.so``,
+built in-tree by ``_build.build()``).  The functions with the C names only
+marshal arguments -- tensors or integer device pointers, a torch stream or a
+raw handle -- and return the C status; all of the computation runs in the
+sm_103a kernel.  There is no fallback: if the library is missing or cannot be
+loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+from . import inputs  # noqa: F401  (seeded input generator)
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn.so")
+
+ATTN_OK = 0
+ATTN_EINVAL = -1
+ATTN_EUNSUPPORTED = -2
+ATTN_EALIGN = -3
+ATTN_ECUDA = -4
+ATTN_EDEVICE = -5
+
+# Symbols declared in include/attn.h.
+EXPORTS = ("attn_fwd", "attn_check_device", "attn_status_str", "attn_abi_version")
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str = "attn_fwd"):
+        super().__init__("%s failed: %s (%d)" % (what, attn_status_str(status), status))
+        self.status = status
+
+
+def load_library():
+    """Load libattn.so (raises if it is missing: there is no other path)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libattn.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i = ctypes.c_void_p, ctypes.c_int
+    lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, vp, vp]
+    lib.attn_fwd.restype = i
+    lib.attn_check_device.argtypes = [vp]
+    lib.attn_check_device.restype = i
+    lib.attn_status_str.argtypes = [i]
+    lib.attn_status_str.restype = ctypes.c_char_p
+    lib.attn_abi_version.argtypes = []
+    lib.attn_abi_version.restype = i
+    _lib = lib
+    return lib
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return int(torch.cuda.current_stream().cuda_stream) if torch.cuda.is_available() else None
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def attn_fwd(q, k, v, out, lse, B: int, H: int, N: int, d: int, scale: float, causal,
+             key_lens=None, stream=None) -> int:
+    """The C ``attn_fwd``: pointers (tensors or ints), sizes, flags; returns the status."""
+    lib = load_library()
+    return lib.attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B), int(H), int(N), int(d),
+                        float(scale), 1 if causal else 0, _ptr(key_lens), _stream(stream))
+
+
+def attn_check_device(stream=None) -> int:
+    return load_library().attn_check_device(_stream(stream))
+
+
+def attn_status_str(status: int) -> str:
+    return load_library().attn_status_str(int(status)).decode()
+
+
+def attn_abi_version() -> int:
+    return load_library().attn_abi_version()
+
+
+def attention(q, k, v, causal: bool = False, key_lens=None, scale: float | None = None, stream=None,
+              out=None, lse=None):
+    """Convenience wrapper over ``attn_fwd`` for torch tensors.
+
+    q, k, v: bf16 CUDA tensors [B, H, N, d], contiguous.  key_lens: int32 CUDA
+    tensor [B] or None.  Allocates ``out`` (bf16) and ``lse`` (fp32) with
+    torch when not given, raises ``AttnError`` on a non-OK status.
+    """
+    import torch
+    B, H, N, d = q.shape
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or tuple(t.shape) != (B, H, N, d):
+            raise ValueError("q, k, v must be contiguous bf16 CUDA tensors of one shape [B, H, N, d]")
+    if key_lens is not None and (key_lens.dtype != torch.int32 or not key_lens.is_cuda or key_lens.numel() != B):
+        raise ValueError("key_lens must be an int32 CUDA tensor of B elements")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = attn_fwd(q, k, v, out, lse, B, H, N, d, scale, causal, key_lens, stream)
+    if st != ATTN_OK:
+        raise AttnError(st)
+    return out, lse

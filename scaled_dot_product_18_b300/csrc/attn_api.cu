@@ -1,0 +1,121 @@
+// C ABI of the attention forward: argument checks on the host, tensor-map
+// encoding, launch, and the device error word.  The operation and every
+// argument are specified in include/attn.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn.h"
+#include "attn_internal.h"
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up through the runtime so the
+// library does not link against libcuda (it loads on machines without a GPU).
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 3-D view [B*H][N][d] of a bf16 tensor, box = 64 head-dim columns x 128 rows
+// x 1 head, 128-byte swizzle (one box row = 128 bytes).  Rows past N read as
+// zeros and are clipped on store, so ragged N needs no padding.
+bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N, int d,
+                     float scale, int causal, const int32_t *key_lens, attn_stream_t stream)
+{
+    if (B < 0 || H < 0 || N < 0) return ATTN_EINVAL;
+    if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_EINVAL;
+    if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+    if (!q || !k || !v || !out) return ATTN_EINVAL;
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    const int64_t q_tiles = (static_cast<int64_t>(N) + 127) / 128;
+    if (bh > INT32_MAX || q_tiles * bh > INT32_MAX) return ATTN_EINVAL;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out)) return ATTN_EALIGN;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_EALIGN;
+    if (key_lens && (reinterpret_cast<uintptr_t>(key_lens) & 3u)) return ATTN_EALIGN;
+
+    CUtensorMap tq, tk, tv, to;
+    if (!make_map(&tq, q, static_cast<int>(bh), N, d) || !make_map(&tk, k, static_cast<int>(bh), N, d) ||
+        !make_map(&tv, v, static_cast<int>(bh), N, d) || !make_map(&to, out, static_cast<int>(bh), N, d))
+        return ATTN_ECUDA;
+
+    sdp18::AttnLaunch a{};
+    a.tm_q = &tq;
+    a.tm_k = &tk;
+    a.tm_v = &tv;
+    a.tm_o = &to;
+    a.lse = lse;
+    a.key_lens = key_lens;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.causal = causal ? 1 : 0;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    const int rc = sdp18::attn_fwd_launch(a);
+    if (rc == -2) return ATTN_EUNSUPPORTED;
+    return rc == 0 ? ATTN_OK : ATTN_ECUDA;
+}
+
+attn_status attn_check_device(attn_stream_t stream)
+{
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ECUDA;
+    int v = 0;
+    if (sdp18::read_and_clear_device_error(&v) != 0) return ATTN_ECUDA;
+    return v != 0 ? ATTN_EDEVICE : ATTN_OK;
+}
+
+const char *attn_status_str(attn_status s)
+{
+    switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_EINVAL: return "ATTN_EINVAL: invalid argument";
+    case ATTN_EUNSUPPORTED: return "ATTN_EUNSUPPORTED: head dimension must be 64 or 128";
+    case ATTN_EALIGN: return "ATTN_EALIGN: tensor pointer not 16-byte aligned";
+    case ATTN_ECUDA: return "ATTN_ECUDA: CUDA error";
+    case ATTN_EDEVICE: return "ATTN_EDEVICE: kernel gave up on a bounded wait";
+    }
+    return "unknown attn_status";
+}
+
+int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,100 @@
+"""The C-ABI library: it loads without a GPU, exports what include/attn.h
+declares, and rejects bad arguments on the host before touching CUDA."""
+import os
+import re
+
+import pytest
+
+import scaled_dot_product_18_b300 as sdp
+from scaled_dot_product_18_b300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return sdp.load_library()
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(attn_\w+)\s*\(", txt, flags=re.M))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"attn_fwd", "attn_check_device", "attn_status_str", "attn_abi_version"} <= names
+    assert names == set(sdp.EXPORTS)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_abi_version_and_status_strings(lib):
+    assert sdp.attn_abi_version() == 1
+    for code in (0, -1, -2, -3, -4, -5):
+        assert sdp.attn_status_str(code).startswith("ATTN_")
+    assert sdp.attn_status_str(7) == "unknown attn_status"
+
+
+# Arguments the host can reject without any CUDA call (pointers are fake
+# integers; nothing is dereferenced on these paths).
+P = 1 << 20  # a 16-byte aligned fake address
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(d=96), sdp.ATTN_EUNSUPPORTED),
+    (dict(d=32), sdp.ATTN_EUNSUPPORTED),
+    (dict(B=-1), sdp.ATTN_EINVAL),
+    (dict(H=-2), sdp.ATTN_EINVAL),
+    (dict(N=-3), sdp.ATTN_EINVAL),
+    (dict(scale=0.0), sdp.ATTN_EINVAL),
+    (dict(scale=-0.125), sdp.ATTN_EINVAL),
+    (dict(scale=float("nan")), sdp.ATTN_EINVAL),
+    (dict(scale=float("inf")), sdp.ATTN_EINVAL),
+    (dict(q=None), sdp.ATTN_EINVAL),
+    (dict(k=None), sdp.ATTN_EINVAL),
+    (dict(v=None), sdp.ATTN_EINVAL),
+    (dict(out=None), sdp.ATTN_EINVAL),
+    (dict(q=P + 8), sdp.ATTN_EALIGN),
+    (dict(k=P + 2), sdp.ATTN_EALIGN),
+    (dict(v=P + 1), sdp.ATTN_EALIGN),
+    (dict(out=P + 4), sdp.ATTN_EALIGN),
+    (dict(lse=P + 2), sdp.ATTN_EALIGN),
+    (dict(key_lens=P + 1), sdp.ATTN_EALIGN),
+    (dict(B=1 << 16, H=1 << 15), sdp.ATTN_EINVAL),          # B*H >= 2^31
+    (dict(B=1 << 12, H=1 << 12, N=1 << 20), sdp.ATTN_EINVAL),  # tile grid >= 2^31
+    (dict(B=0, q=None, k=None, v=None, out=None), sdp.ATTN_OK),  # empty: no-op
+    (dict(N=0), sdp.ATTN_OK),
+    (dict(H=0, d=128), sdp.ATTN_OK),
+])
+def test_host_side_rejections(lib, args, want):
+    a = dict(q=P, k=P, v=P, out=P, lse=None, B=2, H=3, N=5, d=64, scale=0.125, causal=0,
+             key_lens=None, stream=None)
+    a.update(args)
+    st = lib.attn_fwd(a["q"], a["k"], a["v"], a["out"], a["lse"], a["B"], a["H"], a["N"], a["d"],
+                      a["scale"], a["causal"], a["key_lens"], a["stream"])
+    assert st == want, (args, st)
+
+
+def test_binding_raises_without_library(tmp_path, monkeypatch):
+    monkeypatch.setattr(sdp, "_lib", None)
+    monkeypatch.setattr(sdp, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError):
+        sdp.load_library()
+
+
+def test_oracle_not_imported_by_product():
+    # the product package never reaches into the oracle (test infrastructure)
+    pkg = os.path.join(ROOT, "scaled_dot_product_18_b300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                txt = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in txt and "from oracle" not in txt, fn
+                assert "attn_oracle" not in txt, fn

@@ -1,0 +1,153 @@
+"""GPU parity: the CUDA path (through the C ABI) against the fp64 oracle on
+the same seeded inputs, plus exact mask agreement and full-size properties."""
+import numpy as np
+import pytest
+
+import oracle
+from scaled_dot_product_18_b300 import inputs as I
+
+from gpu_util import assert_close, run_cuda
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["c1_b1h2n128d64", "c2_b2h8n100d64_keylens", "c3_b16h12n512d64_keylens_x1.5"]
+LARGE = ["c4_b4h32n4096d128_causal", "c5_b1h32n16384d128_causal"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_full_parity(name):
+    w = I.WORKLOADS[name]
+    x = I.make_inputs(w)
+    O, lse = run_cuda(x.q, x.k, x.v, w.scale, w.causal, x.key_lens)
+    O_ref, lse_ref = oracle.attention_rows(x.q, x.k, x.v, w.scale, w.causal, x.key_lens)
+    assert_close(O, lse, O_ref, lse_ref, name)
+
+
+def _sample_rows(N, rng, n_random=40):
+    fixed = [0, 1, 2, 63, 64, 127, 128, 129, 255, 256, N // 2, N - 129, N - 128, N - 2, N - 1]
+    rows = set(r for r in fixed if 0 <= r < N)
+    rows |= set(rng.integers(0, N, size=n_random).tolist())
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_workload_sampled_parity(name):
+    # Full size, the launch the benchmark times; the oracle computes sampled
+    # rows of sampled heads, and whole-tensor properties cover every row.
+    w = I.WORKLOADS[name]
+    x = I.make_inputs(w)
+    O, lse = run_cuda(x.q, x.k, x.v, w.scale, w.causal, x.key_lens)
+    rng = np.random.default_rng(1234)
+    rows = _sample_rows(w.N, rng)
+    heads = [(0, 0), (w.B - 1, w.H - 1)] + [(int(rng.integers(w.B)), int(rng.integers(w.H))) for _ in range(4)]
+    for b, h in heads:
+        q = x.q[b:b + 1, h:h + 1]
+        k = x.k[b:b + 1, h:h + 1]
+        v = x.v[b:b + 1, h:h + 1]
+        kl = None if x.key_lens is None else x.key_lens[b:b + 1]
+        O_ref, lse_ref = oracle.attention_rows(q, k, v, w.scale, w.causal, kl, rows=rows)
+        assert_close(O[b:b + 1, h:h + 1, rows], lse[b:b + 1, h:h + 1, rows], O_ref, lse_ref, "%s b%d h%d" % (name, b, h))
+    # every row written and finite
+    assert np.isfinite(O).all() and np.isfinite(lse).all()
+    # causal row 0 sees only key 0: O = V[0] exactly (weight 1), lse = s_00
+    v0 = oracle.bf16_to_f64(x.v[:, :, 0])
+    np.testing.assert_array_equal(O[:, :, 0], v0)
+    s00 = w.scale * np.einsum("bhd,bhd->bh", oracle.bf16_to_f64(x.q[:, :, 0]), oracle.bf16_to_f64(x.k[:, :, 0]))
+    assert np.abs(lse[:, :, 0] - s00).max() <= 1e-3
+    # convex combination of V rows: every output lies inside the V range
+    assert O.max() <= oracle.bf16_to_f64(x.v).max() + 1e-2 and O.min() >= oracle.bf16_to_f64(x.v).min() - 1e-2
+
+
+EDGE_N = [1, 2, 63, 64, 65, 127, 128, 129, 255, 257]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_edge_grid(d, causal):
+    for N in EDGE_N:
+        for kl0 in sorted({1, max(N - 1, 1), N}):
+            B, H = 2, 2
+            seed = 1000 * N + kl0 + (7 if causal else 0) + d
+            q = I.make_tensor_bits(seed, I.STREAM_Q, (B, H, N, d))
+            k = I.make_tensor_bits(seed, I.STREAM_K, (B, H, N, d))
+            v = I.make_tensor_bits(seed, I.STREAM_V, (B, H, N, d))
+            kl = np.array([kl0, N], dtype=np.int32)
+            scale = 1.0 / np.sqrt(d)
+            O, lse = run_cuda(q, k, v, scale, causal, kl)
+            O_ref, lse_ref = oracle.attention_rows(q, k, v, scale, causal, kl)
+            assert_close(O, lse, O_ref, lse_ref, "N=%d key_len=%d d=%d causal=%s" % (N, kl0, d, causal))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_len_zero_gives_zero_and_minus_inf(causal):
+    B, H, N, d = 3, 2, 130, 64
+    q, k, v = (I.make_tensor_bits(5, s, (B, H, N, d)) for s in (0, 1, 2))
+    kl = np.array([0, 77, 130], dtype=np.int32)
+    O, lse = run_cuda(q, k, v, 0.125, causal, kl)
+    assert np.all(O[0] == 0.0) and np.all(np.isneginf(lse[0]))
+    O_ref, lse_ref = oracle.attention_rows(q, k, v, 0.125, causal, kl)
+    assert_close(O, lse, O_ref, lse_ref, "key_len 0")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_mask_probe_exact(d, causal):
+    # With V[j] = e_j (one-hot, N <= d) the output row i is row i of the
+    # softmax matrix P itself: hidden keys must get exactly 0, visible keys a
+    # positive weight.  Exact agreement on which positions are masked.
+    N = min(d, 100)
+    B, H = 2, 2
+    q, k = (I.make_tensor_bits(9, s, (B, H, N, d)) for s in (0, 1))
+    eye = np.zeros((N, d))
+    eye[np.arange(N), np.arange(N)] = 1.0
+    from scaled_dot_product_18_b300.inputs import f64_to_bf16_bits
+    v = np.broadcast_to(f64_to_bf16_bits(eye), (B, H, N, d)).copy()
+    kl = np.array([37, N], dtype=np.int32)
+    O, lse = run_cuda(q, k, v, 1.0 / np.sqrt(d), causal, kl)
+    for b in range(B):
+        keep = oracle.visible_mask(N, causal, int(kl[b]))
+        Pg = O[b, :, :, :N]
+        assert np.all(Pg[:, ~keep] == 0.0), "weight on a hidden key"
+        assert np.all(Pg[:, keep] > 0.0), "zero weight on a visible key"
+        assert np.all(O[b, :, :, N:] == 0.0)
+    O_ref, lse_ref = oracle.attention_rows(q, k, v, 1.0 / np.sqrt(d), causal, kl)
+    assert_close(O, lse, O_ref, lse_ref, "one-hot probe")
+
+
+def test_large_logits_and_lazy_rescale():
+    # Key norms grow along the sequence so each row's running max keeps rising
+    # across key tiles (the rescale path), with logits far beyond exp's range.
+    B, H, N, d = 1, 4, 640, 128
+    base_q = oracle.bf16_to_f64(I.make_tensor_bits(21, 0, (B, H, N, d)))
+    base_k = oracle.bf16_to_f64(I.make_tensor_bits(21, 1, (B, H, N, d)))
+    ramp = (1.0 + 6.0 * np.arange(N) / N)[None, None, :, None]
+    from scaled_dot_product_18_b300.inputs import f64_to_bf16_bits
+    q = f64_to_bf16_bits(base_q * 3.0)
+    k = f64_to_bf16_bits(base_k * ramp)
+    v = I.make_tensor_bits(21, 2, (B, H, N, d))
+    for causal in (False, True):
+        O, lse = run_cuda(q, k, v, 1.0 / np.sqrt(d), causal)
+        O_ref, lse_ref = oracle.attention_rows(q, k, v, 1.0 / np.sqrt(d), causal)
+        assert np.abs(lse_ref).max() > 50  # far outside exp's fp32 range without the max shift
+        assert_close(O, lse, O_ref, lse_ref, "large logits causal=%s" % causal)
+
+
+def test_custom_scale_no_lse_and_side_stream():
+    import torch
+    B, H, N, d = 2, 3, 300, 128
+    q, k, v = (I.make_tensor_bits(31, s, (B, H, N, d)) for s in (0, 1, 2))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        O, lse = run_cuda(q, k, v, 0.3, True, None, with_lse=False, stream=s)
+    assert lse is None
+    O_ref, _ = oracle.attention_rows(q, k, v, 0.3, True)
+    assert_close(O, None, O_ref, None, "scale 0.3, no lse, side stream")
+
+
+def test_deterministic():
+    B, H, N, d = 1, 4, 1000, 128
+    q, k, v = (I.make_tensor_bits(41, s, (B, H, N, d)) for s in (0, 1, 2))
+    O1, l1 = run_cuda(q, k, v, 0.1, True)
+    O2, l2 = run_cuda(q, k, v, 0.1, True)
+    np.testing.assert_array_equal(O1, O2)
+    np.testing.assert_array_equal(l1, l2)
