@@ -1,0 +1,355 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention forward on B300 (one JSON line on stdout).
+
+A step is one attn_fwd call over the whole workload (default: B=1, H=32,
+N=16384, d=128, causal -- the long-context shape whose materialised score
+matrix runs out of memory on the pages' A100 example).  Throughput is the
+nominal attention-forward flop count 4*B*H*N^2*d (halved for causal) per
+second.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(independent (batch, head) problems need no exchange: weak scaling); the
+step time is the max over ranks.  ``--impl reference`` times the fp64 CPU
+oracle instead, on a bounded row sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from scaled_dot_product_18_b300 import inputs as I  # noqa: E402
+
+DEFAULT_CONFIG = "c5_b1h32n16384d128_causal"
+NOMINAL_BF16_TFLOPS = 2250.0  # B300 dense BF16, NVIDIA datasheet (context)
+KERNEL_NAME = "attn_fwd_kernel"
+CSRC = os.path.join(ROOT, "scaled_dot_product_18_b300", "csrc")
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for fn in sorted(os.listdir(CSRC)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            h.update(fn.encode())
+            h.update(open(os.path.join(CSRC, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"bf16_tflops": d["bf16_tflops"], "bf16_tflops_sustained": d.get("bf16_tflops_sustained"),
+                "hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "hbm_gbs": 6400.0, "source": "fallback"}
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; otherwise None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(workload)
+        if e and e.get("kernel_src_sha") == kernel_source_sha():
+            return float(e["dram_bytes_per_launch"])
+    except (ValueError, KeyError):
+        pass
+    return None
+
+
+# ----------------------------------------------------------------- clocks
+
+_REASONS = {
+    0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+    0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+    0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
+}
+
+
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running."""
+
+    def __init__(self, device_index: int, period_s: float = 0.02):
+        self.samples, self.reasons = [], 0
+        self.period = period_s
+        self._stop = threading.Event()
+        self.max_mhz = None
+        self.ok = False
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nv = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+            self.ok = True
+        except Exception:  # noqa: BLE001 - clocks are reported as unavailable
+            self._nv = None
+
+    def _run(self):
+        nv = self._nv
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                self.reasons |= int(nv.nvmlDeviceGetCurrentClocksEventReasons(self._h))
+            except Exception:  # noqa: BLE001
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self) -> dict:
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
+        names = [n for bit, n in _REASONS.items() if self.reasons & bit and n != "gpu_idle"]
+        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def oracle_sample(w: I.Workload, x: I.HostInputs, budget_s: float, rows_hint: int | None = None):
+    """Time the fp64 oracle on a stratified row sample of one head, sized to
+    take about ``budget_s`` seconds; returns (flops_per_s, seconds, desc, cores)."""
+    import oracle
+    cores = oracle.default_threads()
+    b, h = 0, 0
+    q = x.q[b:b + 1, h:h + 1]
+    k = x.k[b:b + 1, h:h + 1]
+    v = x.v[b:b + 1, h:h + 1]
+    kl = None if x.key_lens is None else x.key_lens[b:b + 1]
+    per_row_nominal = w.flops() / (w.B * w.H * w.N)
+
+    def rows_for(n):
+        n = max(1, min(n, w.N))
+        return np.floor((np.arange(n) + 0.5) * w.N / n).astype(np.int64)
+
+    if rows_hint is None:
+        oracle.build()
+        oracle.attention_rows(q, k, v, w.scale, w.causal, kl, rows=rows_for(1), threads=1)  # load the library
+        n0 = 4 * max(cores, 8)
+        t0 = time.perf_counter()
+        oracle.attention_rows(q, k, v, w.scale, w.causal, kl, rows=rows_for(n0), threads=cores)
+        dt = max(time.perf_counter() - t0, 1e-4)
+        rows_hint = int(n0 * budget_s / dt)
+    rows = rows_for(rows_hint)
+    t0 = time.perf_counter()
+    oracle.attention_rows(q, k, v, w.scale, w.causal, kl, rows=rows, threads=cores)
+    dt = time.perf_counter() - t0
+    flops = per_row_nominal * rows.size
+    desc = "%d stratified query rows of head (0,0) of %s (nominal %.3g flop/row), %d threads" % (
+        rows.size, w.name, per_row_nominal, cores)
+    return flops / dt, dt, desc, cores, rows.size
+
+
+# ----------------------------------------------------------------- main
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, w, ws, rank):
+    if rank != 0:
+        return 0
+    x = I.make_inputs(w)
+    budget = max(0.5, args.ref_seconds / max(1, args.steps + args.warmup))
+    rate, dt, desc, cores, nrows = oracle_sample(w, x, budget)
+    for _ in range(args.warmup):
+        oracle_sample(w, x, budget, rows_hint=nrows)
+    rates, times = [], []
+    for _ in range(args.steps):
+        r, t, desc, cores, nrows = oracle_sample(w, x, budget, rows_hint=nrows)
+        rates.append(r)
+        times.append(t)
+    value = statistics.median(rates) / 1e12
+    line = {
+        "impl": "reference", "metric": "attention_fwd_tflops", "value": value, "unit": "TFLOPS",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * statistics.median(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "step": "bounded row sample of the workload (see cpu_baseline.sample)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main() -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=I.WORKLOAD_ORDER)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
+    ap.add_argument("--ref-seconds", type=float, default=60.0, help="reference-arm total budget")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = I.WORKLOADS[args.config]
+    ws, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        return run_reference(args, w, ws, rank)
+
+    import torch
+    import torch.distributed as dist
+
+    import scaled_dot_product_18_b300 as sdp
+    sdp.load_library()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    x = I.make_inputs(w)
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(torch.bfloat16)  # noqa: E731
+    q, k, v = dev(x.q), dev(x.k), dev(x.v)
+    kl = torch.from_numpy(x.key_lens).cuda() if x.key_lens is not None else None
+    out = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def step():
+        st = sdp.attn_fwd(q, k, v, out, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, kl, sh)
+        if st != sdp.ATTN_OK:
+            raise sdp.AttnError(st)
+
+    for _ in range(args.warmup):
+        step()
+    st = sdp.attn_check_device(sh)
+    if st != sdp.ATTN_OK:
+        raise sdp.AttnError(st, "warm-up")
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    # ------------------------------------------------ device-resident timing
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device())
+    barrier()
+    torch.cuda.synchronize()
+    with sampler:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    barrier()
+    ms_total = e0.elapsed_time(e1)
+    if ws > 1:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    st = sdp.attn_check_device(sh)
+    if st != sdp.ATTN_OK:
+        raise sdp.AttnError(st, "timed steps")
+    if not bool(torch.isfinite(out).all()) or not bool(torch.isfinite(lse).all()):
+        raise RuntimeError("non-finite output")
+    ms_step = ms_total / args.steps
+    flops = w.flops()
+    value = flops * ws / (ms_step * 1e-3) / 1e12
+
+    # ------------------------------------------------ end to end (host buffers)
+    hq, hk, hv = (torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory() for b in (x.q, x.k, x.v))
+    hkl = torch.from_numpy(x.key_lens).pin_memory() if x.key_lens is not None else None
+    hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        if kl is not None:
+            kl.copy_(hkl, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = e2.elapsed_time(e3) / args.e2e_steps
+    if ws > 1:
+        t = torch.tensor([ms_e2e], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    h2d = 3 * q.numel() * 2 + (kl.numel() * 4 if kl is not None else 0)
+    d2h = out.numel() * 2 + lse.numel() * 4
+
+    peaks = measured_peaks()
+    achieved = flops / (ms_step * 1e-3) / 1e12  # one launch per step
+    traffic = committed_traffic(w.name)
+    line = {
+        "metric": "attention_fwd_tflops", "value": value, "unit": "TFLOPS", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "key_lens": list(w.key_len_range) if w.key_len_range else None,
+                   "flops_per_step": flops, "parallelism": "replica per GPU" if ws > 1 else "single GPU",
+                   "l2": "inputs larger than L2" if w.algorithmic_bytes() > 126e6 else "inputs fit in L2 (no flush)"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                     "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
+                     "frac_of_nominal_2250": achieved / NOMINAL_BF16_TFLOPS,
+                     "achieved_gbs": w.algorithmic_bytes() / (ms_step * 1e-3) / 1e9,
+                     "algorithmic_bytes": w.algorithmic_bytes(), "kernel": KERNEL_NAME},
+        "e2e": {"value": flops * ws / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+        "kernel_src_sha": kernel_source_sha(),
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rate, dt, desc, cores, _ = oracle_sample(w, x, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -239,7 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q_abs = q0 + row;
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
         float m = -INFINITY;  // running max of scale*log2(e)*s used for P
-        float l = 0.f;        // running sum of P (fp32, before bf16 rounding)
+        float l = 0.f;        // running sum of P in fp32 (exact weights: gives the LSE)
+        float l_mma = 0.f;    // running sum of P as rounded to bf16 for the PV MMA
         bool ok = true;
         // The TMEM loads/stores below are warp-collective, so a wait's outcome
         // is made warp-uniform by a vote.
@@ -301,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float neg_m = -m;
             uint32_t pk[kBN / 2];
-            float sum0 = 0.f, sum1 = 0.f;
+            float sum0 = 0.f, sum1 = 0.f, rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
             for (int c = 0; c < kBN / 2; ++c) {
                 const float p0 = ex2(fmaf(s[2 * c], scale_log2, neg_m));
@@ -309,8 +310,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sum0 += p0;
                 sum1 += p1;
                 pk[c] = pack_bf16x2(p0, p1);
+                // the bf16 values the MMA multiplies V by, widened exactly
+                rs0 += __uint_as_float(pk[c] << 16);
+                rs1 += __uint_as_float(pk[c] & 0xFFFF0000u);
             }
             l = l * alpha + (sum0 + sum1);
+            // O is normalised by the sum of the weights it was built from, so
+            // O / l_mma is an exact convex combination of V rows up to the
+            // bf16 rounding of their relative sizes.
+            l_mma = l_mma * alpha + (rs0 + rs1);
 
             if (j > 0) {
                 // P_{j-1} V_{j-1} must be done: it frees the P tile and O is
@@ -353,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
             }
             if (ok) {
-                const float inv_l = have ? 1.f / l : 0.f;
+                const float inv_l = have ? 1.f / l_mma : 0.f;
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
