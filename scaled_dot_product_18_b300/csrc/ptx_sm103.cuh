@@ -95,7 +95,7 @@ enum : int {
 
 // Each wait gives up after this long; a whole forward launch takes
 // milliseconds, so reaching it means a lost arrival, never a slow GPU.
-constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
 constexpr uint64_t kDrainLimitNs = 500000000ull;
 
 // Slow path of a bounded wait: spin with a time limit and an abort flag
