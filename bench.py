@@ -17,12 +17,12 @@ oracle instead, on a bounded row sample of the same workload.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
 import statistics
 import sys
-import threading
 import time
 
 import numpy as np
@@ -74,95 +74,121 @@ def committed_traffic(workload: str):
 
 # ----------------------------------------------------------------- clocks
 
-_REASONS = {
-    0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
-    0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
-    0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting",
-}
+_SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+_REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
 
 class ClockSampler:
-    """Samples SM clock and clock-event reasons through NVML while running."""
+    """Samples the SM clock, power and clock-event reasons of one GPU with
+    ``nvidia-smi -lms`` while the timed region runs (read-only queries)."""
 
-    def __init__(self, device_index: int, period_s: float = 0.02):
-        self.samples, self.reasons = [], 0
-        self.period = period_s
-        self._stop = threading.Event()
-        self.max_mhz = None
-        self.ok = False
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nv = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:  # noqa: BLE001 - clocks are reported as unavailable
-            self._nv = None
-
-    def _run(self):
-        nv = self._nv
-        while not self._stop.is_set():
-            try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                self.reasons |= int(nv.nvmlDeviceGetCurrentClocksEventReasons(self._h))
-            except Exception:  # noqa: BLE001
-                pass
-            time.sleep(self.period)
+    def __init__(self, device_uuid: str | None, period_ms: int = 100):
+        self.uuid = device_uuid
+        self.period_ms = period_ms
+        self.proc = None
+        self.lines: list[str] = []
 
     def __enter__(self):
-        if self.ok:
-            self._t = threading.Thread(target=self._run, daemon=True)
-            self._t.start()
+        import shutil
+        import subprocess
+        smi = shutil.which("nvidia-smi")
+        if smi is None:
+            return self
+        cmd = [smi, "--query-gpu=" + _SMI_FIELDS, "--format=csv,noheader,nounits", "-lms", str(self.period_ms)]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)  # let the first sample land before the timed region
         return self
 
     def __exit__(self, *exc):
-        if self.ok:
-            self._stop.set()
-            self._t.join()
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:  # noqa: BLE001
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
     def summary(self) -> dict:
-        if not self.ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unavailable"]}
-        names = [n for bit, n in _REASONS.items() if self.reasons & bit and n != "gpu_idle"]
-        return {"sm_mhz": float(statistics.median(self.samples)), "sm_max_mhz": self.max_mhz,
-                "reasons": names, "samples": len(self.samples)}
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), f[2], int(f[3], 16) if f[3].startswith("0x") else 0,
+                             f[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        # samples taken while the GPU was busy (the SM clock is raised under load)
+        busy = [r for r in rows if not (r[3] & 0x1)] or rows
+        reasons = set()
+        for r in busy:
+            for bit, name in _REASON_BITS.items():
+                if r[3] & bit:
+                    reasons.add(name)
+            for name, flag in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"),
+                                  r[4]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        power = [float(r[2]) for r in busy if r[2].replace(".", "", 1).isdigit()]
+        return {"sm_mhz": float(statistics.median(r[0] for r in busy)), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(busy),
+                "power_w_max": max(power) if power else None}
 
 
 # ----------------------------------------------------------------- CPU oracle
 
-def oracle_sample(w: I.Workload, x: I.HostInputs, budget_s: float, rows_hint: int | None = None):
-    """Time the fp64 oracle on a stratified row sample of one head, sized to
-    take about ``budget_s`` seconds; returns (flops_per_s, seconds, desc, cores)."""
+def oracle_sample(w: I.Workload, x: I.HostInputs, budget_s: float, shape_hint=None):
+    """Time the fp64 oracle on a bounded sample of the workload: the first
+    ``nh`` heads of batch 0, ``nr`` evenly spaced query rows in each, sized to
+    take about ``budget_s`` seconds.  Returns (flops_per_s, seconds, desc,
+    cores, (nh, nr)); flops are the nominal per-row share of ``w.flops()``."""
     import oracle
     cores = oracle.default_threads()
-    b, h = 0, 0
-    q = x.q[b:b + 1, h:h + 1]
-    k = x.k[b:b + 1, h:h + 1]
-    v = x.v[b:b + 1, h:h + 1]
-    kl = None if x.key_lens is None else x.key_lens[b:b + 1]
     per_row_nominal = w.flops() / (w.B * w.H * w.N)
+    kl = None if x.key_lens is None else x.key_lens[:1]
 
-    def rows_for(n):
-        n = max(1, min(n, w.N))
-        return np.floor((np.arange(n) + 0.5) * w.N / n).astype(np.int64)
-
-    if rows_hint is None:
-        oracle.build()
-        oracle.attention_rows(q, k, v, w.scale, w.causal, kl, rows=rows_for(1), threads=1)  # load the library
-        n0 = 4 * max(cores, 8)
+    def run(nh, nr):
+        rows = np.floor((np.arange(nr) + 0.5) * w.N / nr).astype(np.int64)
+        q, k, v = x.q[:1, :nh], x.k[:1, :nh], x.v[:1, :nh]
         t0 = time.perf_counter()
-        oracle.attention_rows(q, k, v, w.scale, w.causal, kl, rows=rows_for(n0), threads=cores)
-        dt = max(time.perf_counter() - t0, 1e-4)
-        rows_hint = int(n0 * budget_s / dt)
-    rows = rows_for(rows_hint)
-    t0 = time.perf_counter()
-    oracle.attention_rows(q, k, v, w.scale, w.causal, kl, rows=rows, threads=cores)
-    dt = time.perf_counter() - t0
-    flops = per_row_nominal * rows.size
-    desc = "%d stratified query rows of head (0,0) of %s (nominal %.3g flop/row), %d threads" % (
-        rows.size, w.name, per_row_nominal, cores)
-    return flops / dt, dt, desc, cores, rows.size
+        oracle.attention_rows(q, k, v, w.scale, w.causal, kl, rows=rows, threads=cores)
+        return time.perf_counter() - t0
+
+    def split(total_rows):
+        total_rows = max(1, min(int(total_rows), w.H * w.N))
+        nh = max(1, min(w.H, -(-total_rows // w.N)))
+        return nh, max(1, min(w.N, total_rows // nh))
+
+    if shape_hint is None:
+        oracle.build()
+        nh, nr = split(8 * cores)
+        run(nh, nr)  # loads the library, warms the caches
+        for _ in range(4):  # grow the sample until one run takes a good share of the budget
+            dt = max(run(nh, nr), 1e-4)
+            want = nh * nr * budget_s / dt
+            nh, nr = split(want)
+            if dt > 0.3 * budget_s:
+                break
+        shape_hint = (nh, nr)
+    nh, nr = shape_hint
+    dt = run(nh, nr)
+    flops = per_row_nominal * nh * nr
+    desc = ("%d evenly spaced query rows in each of heads 0..%d of batch 0 of %s (nominal %.3g flop/row, "
+            "%d rows), fp64, %d threads" % (nr, nh - 1, w.name, per_row_nominal, nh * nr, cores))
+    return flops / dt, dt, desc, cores, (nh, nr)
 
 
 # ----------------------------------------------------------------- main
@@ -179,12 +205,12 @@ def run_reference(args, w, ws, rank):
         return 0
     x = I.make_inputs(w)
     budget = max(0.5, args.ref_seconds / max(1, args.steps + args.warmup))
-    rate, dt, desc, cores, nrows = oracle_sample(w, x, budget)
+    rate, dt, desc, cores, shp = oracle_sample(w, x, budget)
     for _ in range(args.warmup):
-        oracle_sample(w, x, budget, rows_hint=nrows)
+        oracle_sample(w, x, budget, shape_hint=shp)
     rates, times = [], []
     for _ in range(args.steps):
-        r, t, desc, cores, nrows = oracle_sample(w, x, budget, rows_hint=nrows)
+        r, t, desc, cores, shp = oracle_sample(w, x, budget, shape_hint=shp)
         rates.append(r)
         times.append(t)
     value = statistics.median(rates) / 1e12
@@ -205,7 +231,7 @@ def run_reference(args, w, ws, rank):
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default=DEFAULT_CONFIG, choices=I.WORKLOAD_ORDER)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
@@ -213,10 +239,16 @@ def main() -> int:
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
     ap.add_argument("--ref-seconds", type=float, default=60.0, help="reference-arm total budget")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None, help="override B (smaller cases for profiling)")
+    ap.add_argument("--heads", type=int, default=None, help="override H (smaller cases for profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = I.WORKLOADS[args.config]
+    if args.batch is not None or args.heads is not None:
+        B = w.B if args.batch is None else args.batch
+        H = w.H if args.heads is None else args.heads
+        w = dataclasses.replace(w, name="%s@B%dH%d" % (w.name, B, H), B=B, H=H)
     ws, rank, local = dist_setup()
 
     if args.impl == "reference":
@@ -257,7 +289,11 @@ def main() -> int:
 
     # ------------------------------------------------ device-resident timing
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(torch.cuda.current_device())
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:  # noqa: BLE001 - sample every visible GPU instead
+        uuid = None
+    sampler = ClockSampler(uuid)
     barrier()
     torch.cuda.synchronize()
     with sampler:
