@@ -120,7 +120,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
 
     // Heaviest causal pairs (largest query index) first: the grid is ordered
     // by descending query pair, all heads of one pair together.
@@ -158,27 +157,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // The producer and MMA warps run their loops with all 32 lanes (waits
+    // agreed by a vote); one elected lane issues each copy, MMA and commit.
+    auto wait_warp = [&](uint32_t b_addr, uint32_t parity, int site) -> bool {
+        return __all_sync(0xffffffffu, wait_bounded(b_addr, parity, abort_flag, site, &g_sdp18_error));
+    };
+
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ producer
-        if (lane == 0 && n_max > 0) {
+        if (n_max > 0) {
             tma_prefetch_map(&tm_q);
             tma_prefetch_map(&tm_k);
             tma_prefetch_map(&tm_v);
             const int q_tiles = n1 > 0 ? 2 : 1;  // tile 0 has keys whenever tile 1 has
-            mbar_arrive_expect_tx(bar(L::kBarQFull), q_tiles * L::kQBytes);
+            mbar_arrive_expect_tx_one(bar(L::kBarQFull), q_tiles * L::kQBytes);
             for (int t = 0; t < q_tiles; ++t)
                 for (int cb = 0; cb < D / 64; ++cb)
-                    tma_load_3d(sQ(t) + cb * kBM * 128, &tm_q, bar(L::kBarQFull), cb * 64, q0 + t * kBM, bh);
+                    tma_load_3d_one(sQ(t) + cb * kBM * 128, &tm_q, bar(L::kBarQFull), cb * 64, q0 + t * kBM, bh);
             int issued = 0;
             for (int item = 0; item < 2 * n_max; ++item) {
                 const int s = item % L::kNumSlots;
                 const uint32_t round = static_cast<uint32_t>(item / L::kNumSlots);
-                if (!wait_bounded(bar(L::kBarEmpty + s), (round & 1) ^ 1, abort_flag, 1, &g_sdp18_error)) break;
+                if (!wait_warp(bar(L::kBarEmpty + s), (round & 1) ^ 1, 1)) break;
                 const CUtensorMap *map = (item & 1) ? &tm_v : &tm_k;
                 const uint32_t dst = sRing + s * L::kKVBytes;
-                mbar_arrive_expect_tx(bar(L::kBarFull + s), L::kKVBytes);
+                mbar_arrive_expect_tx_one(bar(L::kBarFull + s), L::kKVBytes);
                 for (int cb = 0; cb < D / 64; ++cb)
-                    tma_load_3d(dst + cb * kBN * 128, map, bar(L::kBarFull + s), cb * 64, (item >> 1) * kBN, bh);
+                    tma_load_3d_one(dst + cb * kBN * 128, map, bar(L::kBarFull + s), cb * 64, (item >> 1) * kBN, bh);
                 ++issued;
             }
             // Copies must have landed before the CTA's shared memory goes away.
@@ -188,13 +193,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && n_max > 0) {
+        if (n_max > 0) {
             constexpr uint32_t kIdescS = idesc_bf16_f32(kBM, kBN, false);
             constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, true);
+            const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);  // warp-uniform
             const int n_t[2] = {n0, n1};
             auto wait_full = [&](int item, int site) -> bool {
-                const bool r = wait_bounded(bar(L::kBarFull + item % L::kNumSlots), (item / L::kNumSlots) & 1,
-                                            abort_flag, site, &g_sdp18_error);
+                const bool r = wait_warp(bar(L::kBarFull + item % L::kNumSlots), (item / L::kNumSlots) & 1, site);
                 tc_fence_after();
                 return r;
             };
@@ -206,9 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t off = (kk >> 2) * (kBM * 128) + (kk & 3) * 32;
                     const uint64_t a = sdesc_sw128(sQ(t) + off, 16, 1024);
                     const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * (kBN * 128) + (kk & 3) * 32, 16, 1024);
-                    mma_bf16_ss(tmem + kTmemS + t * kBN, a, bd, kIdescS, kk > 0 ? 1u : 0u);
+                    mma_bf16_ss_one(tm + kTmemS + t * kBN, a, bd, kIdescS, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(bar(L::kBarSFull + t));
+                mma_commit_one(bar(L::kBarSFull + t));
             };
             // O_t (+)= P_t V from the V tile in ring slot `vs`; P_t is read
             // from TMEM, 16 keys (8 packed columns) per MMA.
@@ -220,17 +225,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // 128 bytes per K step; the next 64 head-dim columns sit one
                     // [128 x 64] block further on (leading byte offset).
                     const uint64_t bd = sdesc_sw128(vbase + kk * 16 * 128, kBN * 128, 1024);
-                    mma_bf16_ts(tmem + kTmemO + t * D, tmem + kTmemS + t * kBN + kk * 8, bd, kIdescPV,
-                                (acc || kk > 0) ? 1u : 0u);
+                    mma_bf16_ts_one(tm + kTmemO + t * D, tm + kTmemS + t * kBN + kk * 8, bd, kIdescPV,
+                                    (acc || kk > 0) ? 1u : 0u);
                 }
             };
 
-            bool ok = wait_bounded(bar(L::kBarQFull), 0, abort_flag, 2, &g_sdp18_error);
+            bool ok = wait_warp(bar(L::kBarQFull), 0, 2);
             if (ok) ok = wait_full(0, 3);
             if (ok) {
                 for (int t = 0; t < 2; ++t)
                     if (n_t[t] > 0) issue_s(t, 0);
-                mma_commit(bar(L::kBarEmpty + 0));
+                mma_commit_one(bar(L::kBarEmpty + 0));
             }
             for (int j = 0; j < n_max && ok; ++j) {
                 const int v_item = 2 * j + 1, k_item = 2 * j + 2;
@@ -239,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 bool k_ready = false;
                 for (int t = 0; t < 2 && ok; ++t) {
                     if (j >= n_t[t]) continue;
-                    ok = wait_bounded(bar(L::kBarPFull + t), j & 1, abort_flag, 5 + t, &g_sdp18_error);
+                    ok = wait_warp(bar(L::kBarPFull + t), j & 1, 5 + t);
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv(t, vs, j > 0);
@@ -251,15 +256,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         issue_s(t, ks);
                     } else {
-                        mma_commit(bar(L::kBarODone + t));
+                        mma_commit_one(bar(L::kBarODone + t));
                     }
                 }
                 if (!ok) break;
-                mma_commit(bar(L::kBarEmpty + vs));
-                if (k_ready) mma_commit(bar(L::kBarEmpty + ks));
+                mma_commit_one(bar(L::kBarEmpty + vs));
+                if (k_ready) mma_commit_one(bar(L::kBarEmpty + ks));
             }
             // Every MMA must be finished before TMEM is released.
-            mma_commit(bar(L::kBarDrain));
+            mma_commit_one(bar(L::kBarDrain));
             wait_drain(bar(L::kBarDrain), 0);
         }
     } else {
@@ -276,11 +281,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l = 0.f;        // running sum of P in fp32 (exact weights: gives the LSE)
         float l_o = 0.f;      // running sum of P as rounded to bf16 for the P V MMA
         bool ok = true;
-        // TMEM loads/stores are warp-collective, so a wait's outcome is made
-        // warp-uniform by a vote.
-        auto wait_warp = [&](uint32_t b_addr, uint32_t parity, int site) -> bool {
-            return __all_sync(0xffffffffu, wait_bounded(b_addr, parity, abort_flag, site, &g_sdp18_error));
-        };
         const float2 sl2 = make_float2(scale_log2, scale_log2);
 
         for (int j = 0; j < n_kv; ++j) {
