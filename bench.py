@@ -193,6 +193,24 @@ def oracle_sample(w: I.Workload, x: I.HostInputs, budget_s: float, shape_hint=No
 
 # ----------------------------------------------------------------- main
 
+def max_over_ranks(ms: float, ws: int, device=None) -> float:
+    """The slowest rank's time: every rank's timed region is bracketed by the
+    same barriers, so the job took as long as its slowest rank."""
+    if ws <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, ws: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank runs its own replica of the workload
+    (independent (batch, head) problems, weak scaling)."""
+    return flops_per_rank * ws / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -303,11 +321,7 @@ def main() -> int:
         e1.record(stream)
         torch.cuda.synchronize()
     barrier()
-    ms_total = e0.elapsed_time(e1)
-    if ws > 1:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(e0.elapsed_time(e1), ws, "cuda")
     st = sdp.attn_check_device(sh)
     if st != sdp.ATTN_OK:
         raise sdp.AttnError(st, "timed steps")
@@ -315,7 +329,7 @@ def main() -> int:
         raise RuntimeError("non-finite output")
     ms_step = ms_total / args.steps
     flops = w.flops()
-    value = flops * ws / (ms_step * 1e-3) / 1e12
+    value = job_tflops(flops, ws, ms_step)
 
     # ------------------------------------------------ end to end (host buffers)
     hq, hk, hv = (torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).pin_memory() for b in (x.q, x.k, x.v))
@@ -345,11 +359,7 @@ def main() -> int:
     e3.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms_e2e = e2.elapsed_time(e3) / args.e2e_steps
-    if ws > 1:
-        t = torch.tensor([ms_e2e], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(e2.elapsed_time(e3) / args.e2e_steps, ws, "cuda")
     h2d = 3 * q.numel() * 2 + (kl.numel() * 4 if kl is not None else 0)
     d2h = out.numel() * 2 + lse.numel() * 4
 
@@ -370,12 +380,20 @@ def main() -> int:
                      "frac_of_nominal_2250": achieved / NOMINAL_BF16_TFLOPS,
                      "achieved_gbs": w.algorithmic_bytes() / (ms_step * 1e-3) / 1e9,
                      "algorithmic_bytes": w.algorithmic_bytes(), "kernel": KERNEL_NAME},
-        "e2e": {"value": flops * ws / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_tflops(flops, ws, ms_e2e), "unit": "TFLOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
         "gpu_launches": args.steps,
         "clocks": sampler.summary(),
         "kernel_src_sha": kernel_source_sha(),
     }
+    clk = line["clocks"]
+    if clk.get("sm_mhz"):
+        # dense bf16 rate measured on this part: 8192 flop per SM per clock (M=128 tcgen05.mma)
+        clock_peak = 8192.0 * 148 * clk["sm_mhz"] * 1e6 / 1e12
+        line["roofline"]["clock_peak_tflops"] = clock_peak
+        line["roofline"]["frac_of_clock_peak"] = achieved / clock_peak
+    if peaks.get("bf16_tflops_sustained"):
+        line["roofline"]["frac_of_sustained"] = achieved / peaks["bf16_tflops_sustained"]
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         rate, dt, desc, cores, _ = oracle_sample(w, x, args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate / 1e12, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
