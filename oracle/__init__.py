@@ -52,7 +52,7 @@ def _load():
         f = lib.oracle_attn_fwd
         dp = ctypes.POINTER(ctypes.c_double)
         f.argtypes = [dp, dp, dp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
-                      ctypes.c_double, ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                      ctypes.c_double, ctypes.c_int, ctypes.c_int64, ctypes.POINTER(ctypes.c_int32),
                       ctypes.POINTER(ctypes.c_int64), ctypes.c_int64, dp, dp, ctypes.c_int]
         f.restype = ctypes.c_int
         _lib = lib
@@ -77,13 +77,15 @@ def default_threads() -> int:
 
 
 def attention_rows(q, k, v, scale: float, causal: bool, key_lens=None, rows=None,
-                   threads: int | None = None):
+                   threads: int | None = None, window: int = 0):
     """Row-mode oracle.  q: [B, H, Nq, d]; k, v: [B, H, Nk, d] (float64, or
     uint16 bf16 bits).  Query and key positions share one axis from 0, so the
     causal rule is j <= i; self-attention has Nq == Nk.
 
     key_lens: int [B] or None (all keys visible).  rows: query indices to
-    compute (the same for every (b, h)) or None for all.  Returns
+    compute (the same for every (b, h)) or None for all.  window: if > 0,
+    query i sees only keys j > i - window (a sliding window of the last
+    ``window`` positions; aicoding.csdn.net sec. 4.3).  Returns
     ``(O, lse)`` as float64 arrays [B, H, R, d] and [B, H, R].
     """
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
@@ -105,7 +107,7 @@ def attention_rows(q, k, v, scale: float, causal: bool, key_lens=None, rows=None
     lib = _load()
     rc = lib.oracle_attn_fwd(
         q.ctypes.data_as(dp), k.ctypes.data_as(dp), v.ctypes.data_as(dp), B, H, Nq, Nk, d,
-        float(scale), int(bool(causal)),
+        float(scale), int(bool(causal)), int(window),
         kl.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)) if kl is not None else None,
         rows_arr.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)) if rows_arr is not None else None,
         n_rows, out.ctypes.data_as(dp), lse.ctypes.data_as(dp),
@@ -115,8 +117,9 @@ def attention_rows(q, k, v, scale: float, causal: bool, key_lens=None, rows=None
     return out, lse
 
 
-def visible_mask(N: int, causal: bool, key_len: int | None) -> np.ndarray:
-    """[N, N] boolean: key j visible to query i (j < key_len, and j <= i if causal)."""
+def visible_mask(N: int, causal: bool, key_len: int | None, window: int = 0) -> np.ndarray:
+    """[N, N] boolean: key j visible to query i (j < key_len, j <= i if causal,
+    j > i - window if window > 0)."""
     i = np.arange(N)[:, None]
     j = np.arange(N)[None, :]
     keep = np.ones((N, N), dtype=bool)
@@ -124,10 +127,12 @@ def visible_mask(N: int, causal: bool, key_len: int | None) -> np.ndarray:
         keep &= j < key_len
     if causal:
         keep &= j <= i
+    if window > 0:
+        keep &= j > i - window
     return keep
 
 
-def attention_literal(q, k, v, scale: float, causal: bool, key_lens=None):
+def attention_literal(q, k, v, scale: float, causal: bool, key_lens=None, window: int = 0):
     """Materialised-matrix oracle: returns ``(O, lse, P)``, all float64.
 
     S = scale * Q K^T; S[~visible] = -inf; P = softmax(S) along keys; O = P V;
@@ -137,7 +142,7 @@ def attention_literal(q, k, v, scale: float, causal: bool, key_lens=None):
     q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
     B, H, N, d = q.shape
     S = scale * np.matmul(q, np.swapaxes(k, -1, -2))  # [B, H, N, N]
-    keep = np.stack([visible_mask(N, causal, None if key_lens is None else int(key_lens[b]))
+    keep = np.stack([visible_mask(N, causal, None if key_lens is None else int(key_lens[b]), window)
                      for b in range(B)])[:, None]  # [B, 1, N, N]
     S = np.where(keep, S, -np.inf)
     m = S.max(axis=-1, keepdims=True)

@@ -21,7 +21,10 @@
  *   A key j is visible to query i iff j < key_len[b] (key-padding mask,
  *     lshu.cn "Self-attention meets the compute wall", sec. 4.1 and 5.2) and,
  *     when causal, j <= i (only earlier positions and itself; hotelren.com
- *     sec. 2.1 note 2, lshu.cn sec. 3.1).
+ *     sec. 2.1 note 2, lshu.cn sec. 3.1) and, when a sliding window of w > 0
+ *     positions is given, j > i - w (the window of the last w positions up to
+ *     the query; aicoding.csdn.net sec. 4.3, sliding-window attention with
+ *     w = 512, and hotelren.com ch.1, local window attention at O(n w)).
  *
  * For each batch b, head h and query row i:
  *   s_j   = scale * sum_t q[i,t] k[j,t]          (visible j only)
@@ -41,6 +44,7 @@ typedef struct {
     int64_t B, H, Nq, Nk, d;
     double scale;
     int causal;
+    int64_t window;
     const int32_t *key_lens;
     const int64_t *rows;
     int64_t n_rows;
@@ -48,10 +52,11 @@ typedef struct {
     int64_t first, last; /* half-open range of work items (b, h, row) */
 } oracle_job;
 
-static int key_visible(int64_t i, int64_t j, int64_t key_len, int causal)
+static int key_visible(int64_t i, int64_t j, int64_t key_len, int causal, int64_t window)
 {
     if (j >= key_len) return 0;
     if (causal && j > i) return 0;
+    if (window > 0 && j <= i - window) return 0;
     return 1;
 }
 
@@ -71,7 +76,7 @@ static void oracle_row(const oracle_job *jb, int64_t item, double *s)
     double m = -INFINITY;
     int64_t n_visible = 0;
     for (int64_t j = 0; j < N; ++j) {
-        if (!key_visible(i, j, key_len, jb->causal)) continue;
+        if (!key_visible(i, j, key_len, jb->causal, jb->window)) continue;
         double dot = 0.0;
         for (int64_t t = 0; t < d; ++t) dot += q[t] * K[j * d + t];
         s[j] = jb->scale * dot;
@@ -86,7 +91,7 @@ static void oracle_row(const oracle_job *jb, int64_t item, double *s)
     /* pass 2: exponentials, their sum, and the weighted sum of V rows */
     double l = 0.0;
     for (int64_t j = 0; j < N; ++j) {
-        if (!key_visible(i, j, key_len, jb->causal)) continue;
+        if (!key_visible(i, j, key_len, jb->causal, jb->window)) continue;
         const double w = exp(s[j] - m);
         l += w;
         for (int64_t t = 0; t < d; ++t) o[t] += w * V[j * d + t];
@@ -110,6 +115,7 @@ static void *oracle_worker(void *arg)
  * Query i and key j share one position axis starting at 0 (the causal rule
  * j <= i compares them directly); self-attention has Nq == Nk.
  * key_lens: int32 [B] or NULL (all Nk keys visible); used as given.
+ * window: > 0 limits query i to keys j > i - window; <= 0 means no window.
  * rows: the query rows to compute (same for every (b, h)), or NULL for
  *       0..Nq-1 (then n_rows must equal Nq).
  * out: float64 [B, H, n_rows, d]; lse: float64 [B, H, n_rows].
@@ -117,7 +123,7 @@ static void *oracle_worker(void *arg)
  */
 int oracle_attn_fwd(const double *q, const double *k, const double *v,
                     int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t d,
-                    double scale, int causal, const int32_t *key_lens,
+                    double scale, int causal, int64_t window, const int32_t *key_lens,
                     const int64_t *rows, int64_t n_rows,
                     double *out, double *lse, int n_threads)
 {
@@ -140,7 +146,7 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v,
         oracle_job *jb = &jobs[t];
         jb->q = q; jb->k = k; jb->v = v;
         jb->B = B; jb->H = H; jb->Nq = Nq; jb->Nk = Nk; jb->d = d;
-        jb->scale = scale; jb->causal = causal; jb->key_lens = key_lens;
+        jb->scale = scale; jb->causal = causal; jb->window = window; jb->key_lens = key_lens;
         jb->rows = rows; jb->n_rows = n_rows; jb->out = out; jb->lse = lse;
         jb->first = items * t / n_threads;
         jb->last = items * (t + 1) / n_threads;

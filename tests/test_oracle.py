@@ -19,10 +19,10 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "two_key_closed_form.
 MODES = ["rows", "literal"]
 
 
-def run(mode, q, k, v, scale, causal, key_lens=None):
+def run(mode, q, k, v, scale, causal, key_lens=None, window=0):
     if mode == "rows":
-        return oracle.attention_rows(q, k, v, scale, causal, key_lens, threads=2)
-    O, lse, _ = oracle.attention_literal(q, k, v, scale, causal, key_lens)
+        return oracle.attention_rows(q, k, v, scale, causal, key_lens, threads=2, window=window)
+    O, lse, _ = oracle.attention_literal(q, k, v, scale, causal, key_lens, window=window)
     return O, lse
 
 
@@ -227,6 +227,60 @@ def test_bf16_decode_is_exact():
     np.testing.assert_array_equal(oracle.bf16_to_f64(bits), np.array(want))
 
 
+# --- sliding window (query i sees keys j > i - w) --------------------------------
+
+@pytest.mark.parametrize("mode", MODES)
+def test_window_one_causal_is_self_attention_to_own_row(mode):
+    # w = 1 with the causal rule leaves exactly key i for query i.
+    q, k, v = rnd(31, 2, 2, 19, 5)
+    O, lse = run(mode, q, k, v, 0.8, True, window=1)
+    np.testing.assert_allclose(O, v, atol=1e-12)
+    np.testing.assert_allclose(lse, 0.8 * np.einsum("bhid,bhid->bhi", q, k), atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_window_zero_q_gives_mean_over_window(mode):
+    _, k, v = rnd(32, 2, 1, 23, 4)
+    q = np.zeros_like(k)
+    w = 5
+    kl = np.array([23, 17], dtype=np.int32)
+    for causal in (True, False):
+        O, lse = run(mode, q, k, v, 1.3, causal, kl, window=w)
+        for b in range(2):
+            for i in range(23):
+                lo = max(0, i - w + 1)
+                hi = min(i + 1, int(kl[b])) if causal else int(kl[b])
+                if hi <= lo:
+                    assert np.all(O[b, :, i] == 0.0) and np.all(np.isneginf(lse[b, :, i]))
+                    continue
+                np.testing.assert_allclose(O[b, :, i], v[b, :, lo:hi].mean(axis=1), atol=1e-12)
+                np.testing.assert_allclose(lse[b, :, i], math.log(hi - lo), atol=1e-12)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_window_wider_than_sequence_is_no_window(mode):
+    q, k, v = rnd(33, 1, 2, 15, 6)
+    for causal in (False, True):
+        O0, l0 = run(mode, q, k, v, 0.5, causal)
+        for w in (15, 16, 1000):
+            O1, l1 = run(mode, q, k, v, 0.5, causal, window=w)
+            np.testing.assert_array_equal(O0, O1)
+            np.testing.assert_array_equal(l0, l1)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_window_rows_equal_literal_brute_force(causal):
+    q, k, v = rnd(34, 2, 2, 14, 3, scale=2.0)
+    kl = np.array([9, 14], dtype=np.int32)
+    for w in (1, 2, 3, 7, 13):
+        O1, l1 = run("rows", q, k, v, 0.7, causal, kl, window=w)
+        O2, l2 = run("literal", q, k, v, 0.7, causal, kl, window=w)
+        np.testing.assert_allclose(O1, O2, atol=1e-12)
+        np.testing.assert_array_equal(np.isneginf(l1), np.isneginf(l2))
+        fin = np.isfinite(l2)
+        np.testing.assert_allclose(l1[fin], l2[fin], atol=1e-12)
+
+
 def test_bad_arguments_rejected():
     q, k, v = rnd(17, 1, 1, 4, 2)
     with pytest.raises(ValueError):
@@ -237,7 +291,7 @@ def test_bad_arguments_rejected():
 
 def _mutant(kind):
     """A copy of the literal definition with one planted mistake."""
-    def f(q, k, v, scale, causal, key_lens=None):
+    def f(q, k, v, scale, causal, key_lens=None, window=0):
         q, k, v = [np.asarray(x, dtype=np.float64) for x in (q, k, v)]
         B, H, N, d = q.shape
         sc = 1.0 if kind == "no_scale" else scale
@@ -251,6 +305,8 @@ def _mutant(kind):
                 keep[b, 0] &= (i < kl) if kind == "mask_queries" else (j < kl)
             if causal:
                 keep[b, 0] &= (j < i) if kind == "causal_strict" else (j <= i)
+            if window > 0:
+                keep[b, 0] &= (j >= i - window) if kind == "window_off_by_one" else (j > i - window)
         S = np.where(keep, S, -np.inf)
         m = S.max(-1, keepdims=True)
         m = np.where(np.isfinite(m), m, 0.0)
@@ -282,11 +338,13 @@ def _all_pins_pass(fn):
     O, lse = fn(qz, k, v, 0.9, False, np.array([4], dtype=np.int32))
     checks.append(np.allclose(O[0], v[0, :, :4].mean(axis=1, keepdims=True), atol=1e-9)
                   and np.allclose(lse, math.log(4), atol=1e-9))
+    O, lse = fn(q, k, v, 0.8, True, None, window=1)
+    checks.append(np.allclose(O, v, atol=1e-9))
     return all(checks)
 
 
 @pytest.mark.parametrize("kind", ["no_scale", "transposed", "mask_queries", "causal_strict",
-                                  "no_normalise", "log2_lse", "lse_no_max"])
+                                  "no_normalise", "log2_lse", "lse_no_max", "window_off_by_one"])
 def test_pins_catch_planted_mistakes(kind):
     assert _all_pins_pass(_mutant("none"))
     assert not _all_pins_pass(_mutant(kind)), kind
