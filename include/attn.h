@@ -15,7 +15,9 @@
  *   -- hotelren.com sec. 4.1 (FlashAttention-1: tiles of Q and K/V, online
  *      softmax, the n x n score matrix is never written out).
  *
- * Mask: key j is visible to query i iff j < key_lens[b] (a key-padding mask,
+ * attn_fwd_window adds a sliding window (keys j > i - w only).
+ *
+ * Mask (attn_fwd): key j is visible to query i iff j < key_lens[b] (a key-padding mask,
  * lshu.cn "Self-attention meets the compute wall", sec. 4.1 and 5.2) and,
  * when causal != 0, j <= i (only earlier positions and the query itself;
  * hotelren.com sec. 2.1 note 2).  A hidden key gets exactly zero weight.
@@ -82,6 +84,26 @@ attn_status attn_fwd(const void *q, const void *k, const void *v,
                      const int32_t *key_lens, attn_stream_t stream);
 
 /*
+ * attn_fwd_window -- attn_fwd with a sliding window of `window` positions.
+ *
+ * Same arguments, layout, ownership and errors as attn_fwd, plus:
+ * window  : >= 0.  When 0 < window < N, query i additionally sees only keys
+ *           j > i - window: with causal != 0 that is the last `window`
+ *           positions up to and including i (sliding-window attention,
+ *           aicoding.csdn.net "Why does attention stall large-model
+ *           training", sec. 4.3, window w = 512; local window attention at
+ *           O(n w), hotelren.com "AI attention: essence and evolution",
+ *           ch.1 table).  0 or >= N: no window (identical to attn_fwd).
+ *           Negative -> ATTN_EINVAL.  Key tiles outside every row's window
+ *           are not visited.  A row whose window holds no visible key (only
+ *           possible together with key_lens) gets O = 0 and lse = -inf.
+ */
+attn_status attn_fwd_window(const void *q, const void *k, const void *v,
+                            void *out, float *lse,
+                            int B, int H, int N, int d, float scale, int causal,
+                            const int32_t *key_lens, int window, attn_stream_t stream);
+
+/*
  * attn_check_device -- synchronise `stream`, then read and clear the
  * library's device error word on the current device.  Returns ATTN_EDEVICE
  * if a kernel since the last check gave up on a bounded wait (its outputs are
@@ -95,7 +117,7 @@ const char *attn_status_str(attn_status s);
 /* ABI version of this header (bumped on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 1
+#define ATTN_ABI_VERSION 2
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,7 @@ ATTN_ECUDA = -4
 ATTN_EDEVICE = -5
 
 # Symbols declared in include/attn.h.
-EXPORTS = ("attn_fwd", "attn_check_device", "attn_status_str", "attn_abi_version")
+EXPORTS = ("attn_fwd", "attn_fwd_window", "attn_check_device", "attn_status_str", "attn_abi_version")
 
 _lib = None
 
@@ -48,6 +48,8 @@ def load_library():
     vp, i = ctypes.c_void_p, ctypes.c_int
     lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, vp, vp]
     lib.attn_fwd.restype = i
+    lib.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, vp, i, vp]
+    lib.attn_fwd_window.restype = i
     lib.attn_check_device.argtypes = [vp]
     lib.attn_check_device.restype = i
     lib.attn_status_str.argtypes = [i]
@@ -83,6 +85,14 @@ def attn_fwd(q, k, v, out, lse, B: int, H: int, N: int, d: int, scale: float, ca
                         float(scale), 1 if causal else 0, _ptr(key_lens), _stream(stream))
 
 
+def attn_fwd_window(q, k, v, out, lse, B: int, H: int, N: int, d: int, scale: float, causal,
+                    key_lens=None, window: int = 0, stream=None) -> int:
+    """The C ``attn_fwd_window``: ``attn_fwd`` with a sliding window (keys j > i - window)."""
+    lib = load_library()
+    return lib.attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B), int(H), int(N), int(d),
+                               float(scale), 1 if causal else 0, _ptr(key_lens), int(window), _stream(stream))
+
+
 def attn_check_device(stream=None) -> int:
     return load_library().attn_check_device(_stream(stream))
 
@@ -96,11 +106,11 @@ def attn_abi_version() -> int:
 
 
 def attention(q, k, v, causal: bool = False, key_lens=None, scale: float | None = None, stream=None,
-              out=None, lse=None):
+              out=None, lse=None, window: int = 0):
     """Convenience wrapper over ``attn_fwd`` for torch tensors.
 
     q, k, v: bf16 CUDA tensors [B, H, N, d], contiguous.  key_lens: int32 CUDA
-    tensor [B] or None.  Allocates ``out`` (bf16) and ``lse`` (fp32) with
+    tensor [B] or None.  window > 0: sliding window (keys j > i - window).  Allocates ``out`` (bf16) and ``lse`` (fp32) with
     torch when not given, raises ``AttnError`` on a non-OK status.
     """
     import torch
@@ -116,7 +126,10 @@ def attention(q, k, v, causal: bool = False, key_lens=None, scale: float | None 
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    st = attn_fwd(q, k, v, out, lse, B, H, N, d, scale, causal, key_lens, stream)
+    if window:
+        st = attn_fwd_window(q, k, v, out, lse, B, H, N, d, scale, causal, key_lens, window, stream)
+    else:
+        st = attn_fwd(q, k, v, out, lse, B, H, N, d, scale, causal, key_lens, stream)
     if st != ATTN_OK:
         raise AttnError(st)
     return out, lse

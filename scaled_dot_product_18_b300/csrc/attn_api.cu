@@ -52,14 +52,10 @@ bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d)
 
 bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
-}  // namespace
-
-extern "C" {
-
-attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N, int d,
-                     float scale, int causal, const int32_t *key_lens, attn_stream_t stream)
+attn_status forward(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N, int d,
+                    float scale, int causal, const int32_t *key_lens, int window, attn_stream_t stream)
 {
-    if (B < 0 || H < 0 || N < 0) return ATTN_EINVAL;
+    if (B < 0 || H < 0 || N < 0 || window < 0) return ATTN_EINVAL;
     if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_EINVAL;
     if (B == 0 || H == 0 || N == 0) return ATTN_OK;
@@ -89,10 +85,28 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, flo
     a.d = d;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     a.causal = causal ? 1 : 0;
+    a.window = window >= N ? 0 : window;  // a window covering every key is no window
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     const int rc = sdp18::attn_fwd_launch(a);
     if (rc == -2) return ATTN_EUNSUPPORTED;
     return rc == 0 ? ATTN_OK : ATTN_ECUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N, int d,
+                     float scale, int causal, const int32_t *key_lens, attn_stream_t stream)
+{
+    return forward(q, k, v, out, lse, B, H, N, d, scale, causal, key_lens, 0, stream);
+}
+
+attn_status attn_fwd_window(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N,
+                            int d, float scale, int causal, const int32_t *key_lens, int window,
+                            attn_stream_t stream)
+{
+    return forward(q, k, v, out, lse, B, H, N, d, scale, causal, key_lens, window, stream);
 }
 
 attn_status attn_check_device(attn_stream_t stream)

@@ -6,7 +6,10 @@
 // tile, stream the key/value tiles, form S = Q K^T for the pair, fold it into
 // running row statistics (max, sum), accumulate P V, and never write S out.
 // Key tiles that the mask hides completely are not visited (hotelren.com
-// sec. 5, "only load active K/V blocks").
+// sec. 5, "only load active K/V blocks").  An optional sliding window limits
+// query i to keys j > i - w (aicoding.csdn.net "Why does attention stall
+// large-model training", sec. 4.3): each query tile then visits only the key
+// tiles that intersect its rows' windows.
 //
 // How it maps onto sm_103a.  The CTA owns two query tiles, Q0 (rows q0 ..
 // q0+127) and Q1 (rows q0+128 .. q0+255), which share every K/V tile:
@@ -94,12 +97,19 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk)
     return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// Number of key tiles query tile starting at row q0t visits (0 = none).
-__device__ __forceinline__ int key_tiles(int q0t, int N, int kv_len, int causal)
+// Key tiles [first, end) that query tile q0t visits; empty when first >= end.
+// The upper end follows the key length and the causal diagonal of the
+// tile's last row, the lower end the window of its first row.
+struct KeyRange {
+    int first, end;
+    __device__ __forceinline__ int count() const { return end > first ? end - first : 0; }
+};
+__device__ __forceinline__ KeyRange key_range(int q0t, int N, int kv_len, int causal, int window)
 {
-    if (q0t >= N) return 0;
+    if (q0t >= N) return {0, 0};
     const int kv_end = causal ? min(kv_len, q0t + kBM) : kv_len;
-    return (kv_end + kBN - 1) / kBN;
+    const int lo = window > 0 ? max(0, q0t - window + 1) : 0;
+    return {lo / kBN, (kv_end + kBN - 1) / kBN};
 }
 
 template <int D>
@@ -107,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     float *__restrict__ lse, const int32_t *__restrict__ key_lens, int H, int N, int num_q_pairs,
-                    int num_bh, float scale_log2, int causal)
+                    int num_bh, float scale_log2, int causal, int window)
 {
     using L = Smem<D>;
     extern __shared__ uint8_t smem_raw[];
@@ -129,9 +139,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = bh / H;
     int kv_len = N;
     if (key_lens != nullptr) kv_len = min(max(key_lens[b], 0), N);
-    const int n0 = key_tiles(q0, N, kv_len, causal);
-    const int n1 = key_tiles(q0 + kBM, N, kv_len, causal);
-    const int n_max = max(n0, n1);
+    const KeyRange kr[2] = {key_range(q0, N, kv_len, causal, window),
+                            key_range(q0 + kBM, N, kv_len, causal, window)};
+    const int n0 = kr[0].count(), n1 = kr[1].count();
+    // The CTA streams key tiles [j_begin, j_end), the union of both ranges;
+    // a key tile in the union that neither range holds is still streamed and
+    // consumed, so the ring stays in step.
+    const int j_begin = n0 == 0 ? kr[1].first : n1 == 0 ? kr[0].first : min(kr[0].first, kr[1].first);
+    const int j_end = n0 == 0 ? kr[1].end : n1 == 0 ? kr[0].end : max(kr[0].end, kr[1].end);
+    const int n_max = n0 + n1 > 0 ? j_end - j_begin : 0;  // key tiles streamed
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::kBarQFull), 1);
@@ -169,11 +185,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_map(&tm_q);
             tma_prefetch_map(&tm_k);
             tma_prefetch_map(&tm_v);
-            const int q_tiles = n1 > 0 ? 2 : 1;  // tile 0 has keys whenever tile 1 has
-            mbar_arrive_expect_tx_one(bar(L::kBarQFull), q_tiles * L::kQBytes);
-            for (int t = 0; t < q_tiles; ++t)
-                for (int cb = 0; cb < D / 64; ++cb)
-                    tma_load_3d_one(sQ(t) + cb * kBM * 128, &tm_q, bar(L::kBarQFull), cb * 64, q0 + t * kBM, bh);
+            mbar_arrive_expect_tx_one(bar(L::kBarQFull), ((n0 > 0) + (n1 > 0)) * L::kQBytes);
+            for (int t = 0; t < 2; ++t)
+                if ((t == 0 ? n0 : n1) > 0)
+                    for (int cb = 0; cb < D / 64; ++cb)
+                        tma_load_3d_one(sQ(t) + cb * kBM * 128, &tm_q, bar(L::kBarQFull), cb * 64, q0 + t * kBM,
+                                        bh);
             int issued = 0;
             for (int item = 0; item < 2 * n_max; ++item) {
                 const int s = item % L::kNumSlots;
@@ -183,7 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dst = sRing + s * L::kKVBytes;
                 mbar_arrive_expect_tx_one(bar(L::kBarFull + s), L::kKVBytes);
                 for (int cb = 0; cb < D / 64; ++cb)
-                    tma_load_3d_one(dst + cb * kBN * 128, map, bar(L::kBarFull + s), cb * 64, (item >> 1) * kBN, bh);
+                    tma_load_3d_one(dst + cb * kBN * 128, map, bar(L::kBarFull + s), cb * 64,
+                                    (j_begin + (item >> 1)) * kBN, bh);
                 ++issued;
             }
             // Copies must have landed before the CTA's shared memory goes away.
@@ -198,6 +216,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t kIdescPV = idesc_bf16_f32(kBM, D, true);
             const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);  // warp-uniform
             const int n_t[2] = {n0, n1};
+            // Tile t is active at key tile j (0-based in the stream) when its
+            // range holds it; its local iteration index is j - first.
+            const int f_t[2] = {kr[0].first - j_begin, kr[1].first - j_begin};
+            auto active = [&](int t, int j) { return n_t[t] > 0 && j >= f_t[t] && j < f_t[t] + n_t[t]; };
             auto wait_full = [&](int item, int site) -> bool {
                 const bool r = wait_warp(bar(L::kBarFull + item % L::kNumSlots), (item / L::kNumSlots) & 1, site);
                 tc_fence_after();
@@ -233,31 +255,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = wait_warp(bar(L::kBarQFull), 0, 2);
             if (ok) ok = wait_full(0, 3);
             if (ok) {
+#pragma unroll
                 for (int t = 0; t < 2; ++t)
-                    if (n_t[t] > 0) issue_s(t, 0);
+                    if (active(t, 0)) issue_s(t, 0);
                 mma_commit_one(bar(L::kBarEmpty + 0));
             }
             for (int j = 0; j < n_max && ok; ++j) {
                 const int v_item = 2 * j + 1, k_item = 2 * j + 2;
                 const int vs = v_item % L::kNumSlots, ks = k_item % L::kNumSlots;
                 ok = wait_full(v_item, 4);
+                const bool k_next = j + 1 < n_max;  // K_{j+1} is streamed: consume it below
                 bool k_ready = false;
-                for (int t = 0; t < 2 && ok; ++t) {
-                    if (j >= n_t[t]) continue;
-                    ok = wait_warp(bar(L::kBarPFull + t), j & 1, 5 + t);
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
                     if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(t, vs, j > 0);
-                    if (j + 1 < n_t[t]) {
+                    if (active(t, j)) {
+                        const int jj = j - f_t[t];
+                        ok = wait_warp(bar(L::kBarPFull + t), jj & 1, 5 + t);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(t, vs, jj > 0);
+                        if (jj + 1 == n_t[t]) mma_commit_one(bar(L::kBarODone + t));
+                    }
+                    if (k_next && active(t, j + 1)) {
                         if (!k_ready) {
                             ok = wait_full(k_item, 7);
                             if (!ok) break;
                             k_ready = true;
                         }
                         issue_s(t, ks);
-                    } else {
-                        mma_commit_one(bar(L::kBarODone + t));
                     }
+                }
+                if (ok && k_next && !k_ready) {
+                    ok = wait_full(k_item, 7);  // streamed but used by neither tile
+                    k_ready = ok;
                 }
                 if (!ok) break;
                 mma_commit_one(bar(L::kBarEmpty + vs));
@@ -274,6 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q0t = q0 + t * kBM;
         const int q_abs = q0t + row;
         const int n_kv = t == 0 ? n0 : n1;
+        const int j_first = t == 0 ? kr[0].first : kr[1].first;  // first key tile of this query tile
         const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const uint32_t tS = t_lane + kTmemS + t * kBN;
         const uint32_t tO = t_lane + kTmemO + t * D;
@@ -283,21 +315,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         const float2 sl2 = make_float2(scale_log2, scale_log2);
 
-        for (int j = 0; j < n_kv; ++j) {
-            if (!wait_warp(bar(L::kBarSFull + t), j & 1, 10 + t)) {
+        for (int jj = 0; jj < n_kv; ++jj) {
+            const int j = j_first + jj;  // key tile index
+            if (!wait_warp(bar(L::kBarSFull + t), jj & 1, 10 + t)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // Only the last key tile can hold hidden keys (ragged key tail or
-            // the causal diagonal); earlier tiles are fully visible.  Columns
-            // c >= lim of this tile are hidden.
-            const bool last = j == n_kv - 1;
+            // Hidden keys sit in the last key tile (ragged key tail or the
+            // causal diagonal) and, with a window, in the first tiles (keys
+            // j <= i - w).  Columns c of this tile are visible iff
+            // lim_lo <= c < lim.
+            const bool last = jj == n_kv - 1;
             int lim = kBN;
             if (last) {
                 lim = kv_len - j * kBN;
                 if (causal) lim = min(lim, q_abs - j * kBN + 1);
             }
+            const bool lower = window > 0 && j * kBN < q0t + kBM - window;  // some row's window starts here
+            const int lim_lo = q_abs - window + 1 - j * kBN;
             // 64 score columns from TMEM (two 32-column loads), masked.
             auto load64 = [&](int c0, uint32_t (&ra)[32], uint32_t (&rb)[32]) {
                 tmem_ld32(tS + c0, ra);
@@ -310,6 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 32; ++c) {
                         if (c0 + c >= lim) ra[c] = 0xff800000u;  // -inf
                         if (c0 + 32 + c >= lim) rb[c] = 0xff800000u;
+                    }
+                }
+                if (lower) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        if (c0 + c < lim_lo) ra[c] = 0xff800000u;
+                        if (c0 + 32 + c < lim_lo) rb[c] = 0xff800000u;
                     }
                 }
             };
@@ -333,11 +376,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 alpha = ex2(m - t_max);  // 0 on the first tile (m = -inf)
                 m = t_max;
             }
-            const float2 nm2 = make_float2(-m, -m);
+            // A row that has seen no visible key yet keeps m = -inf; its
+            // scores are all -inf too, so any finite shift gives P = 0.
+            const float m_use = m == -INFINITY ? 0.f : m;
+            const float2 nm2 = make_float2(-m_use, -m_use);
 
             // O_t += P_t V_{j-1} is complete (the S_t commit covers it), so O_t
             // can be rescaled here; rows whose max did not move keep alpha = 1.
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -397,7 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
             }
             if (ok) {
-                const float inv_l = have ? 1.f / l_o : 0.f;
+                // Rows with no visible key (l_o = 0) get O = 0 and lse = -inf.
+                const float inv_l = have && l_o > 0.f ? 1.f / l_o : 0.f;
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -420,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (lse != nullptr && q_abs < N) {
-                    const float v = have ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                    const float v = have && l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
                     lse[static_cast<int64_t>(bh) * N + q_abs] = v;
                 }
             }
@@ -460,7 +507,7 @@ int launch(const AttnLaunch &a)
     const unsigned grid = static_cast<unsigned>(num_q_pairs) * static_cast<unsigned>(num_bh);
     attn_fwd_kernel<D><<<grid, kThreads, L::kAlloc, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, a.lse,
                                                                  a.key_lens, a.H, a.N, num_q_pairs, num_bh,
-                                                                 a.scale_log2, a.causal);
+                                                                 a.scale_log2, a.causal, a.window);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -16,6 +16,7 @@ struct AttnLaunch {
     int B, H, N, d;
     float scale_log2;  // scale * log2(e)
     int causal;
+    int window;  // > 0: query i sees keys j > i - window; 0: no window
     cudaStream_t stream;
 };
 

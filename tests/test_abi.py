@@ -29,14 +29,14 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert {"attn_fwd", "attn_check_device", "attn_status_str", "attn_abi_version"} <= names
+    assert {"attn_fwd", "attn_fwd_window", "attn_check_device", "attn_status_str", "attn_abi_version"} <= names
     assert names == set(sdp.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
 
 
 def test_abi_version_and_status_strings(lib):
-    assert sdp.attn_abi_version() == 1
+    assert sdp.attn_abi_version() == 2
     for code in (0, -1, -2, -3, -4, -5):
         assert sdp.attn_status_str(code).startswith("ATTN_")
     assert sdp.attn_status_str(7) == "unknown attn_status"
@@ -80,6 +80,16 @@ def test_host_side_rejections(lib, args, want):
     st = lib.attn_fwd(a["q"], a["k"], a["v"], a["out"], a["lse"], a["B"], a["H"], a["N"], a["d"],
                       a["scale"], a["causal"], a["key_lens"], a["stream"])
     assert st == want, (args, st)
+
+
+@pytest.mark.parametrize("window,want", [(-1, sdp.ATTN_EINVAL), (-100, sdp.ATTN_EINVAL)])
+def test_window_rejections(lib, window, want):
+    st = lib.attn_fwd_window(P, P, P, P, None, 2, 3, 5, 64, 0.125, 1, None, window, None)
+    assert st == want
+
+
+def test_window_empty_problem_is_ok(lib):
+    assert lib.attn_fwd_window(None, None, None, None, None, 0, 3, 5, 64, 0.125, 1, None, 7, None) == sdp.ATTN_OK
 
 
 def test_binding_raises_without_library(tmp_path, monkeypatch):
