@@ -211,6 +211,16 @@ def job_tflops(flops_per_rank: float, ws: int, ms_per_step: float) -> float:
     return flops_per_rank * ws / (ms_per_step * 1e-3) / 1e12
 
 
+def window_flops(w: I.Workload, window: int) -> float:
+    """4*d flops per visible (query, key) pair of a sliding-window workload:
+    query i sees keys max(0, i - window + 1) .. i (causal) or
+    max(0, i - window + 1) .. N-1 (non-causal); no key lengths."""
+    i = np.arange(w.N, dtype=np.float64)
+    lo = np.maximum(0.0, i - window + 1)
+    hi = i + 1 if w.causal else np.full_like(i, w.N)
+    return 4.0 * w.B * w.H * w.d * float(np.sum(hi - lo))
+
+
 def dist_setup():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -246,6 +256,102 @@ def run_reference(args, w, ws, rank):
     return 0
 
 
+def run_decode(args, w: I.DecodeWorkload, ws: int, rank: int, local: int) -> int:
+    """HBM-bound decode: GB/s of K/V cache (plus q, O, lse) moved per call."""
+    import torch
+    import torch.distributed as dist
+
+    import scaled_dot_product_18_b300 as sdp
+    sdp.load_library()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    x = I.make_decode_inputs(w)
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(torch.bfloat16)  # noqa: E731
+    q, k, v = dev(x.q), dev(x.k), dev(x.v)
+    cl = torch.from_numpy(x.key_lens).cuda() if x.key_lens is not None else None
+    out = torch.empty((w.B, w.H, w.d), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda")
+    nbytes = sdp.attn_decode_workspace_size(w.B, w.H, w.L, w.d)
+    wsbuf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def step():
+        st = sdp.attn_decode(q, k, v, out, lse, w.B, w.H, w.L, w.d, w.scale, cl, wsbuf, nbytes, sh)
+        if st != sdp.ATTN_OK:
+            raise sdp.AttnError(st, "attn_decode")
+
+    for _ in range(args.warmup):
+        step()
+    if sdp.attn_check_device(sh) != sdp.ATTN_OK:
+        raise RuntimeError("device error in warm-up")
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:  # noqa: BLE001
+        uuid = None
+    sampler = ClockSampler(uuid)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with sampler:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms_step = max_over_ranks(e0.elapsed_time(e1), ws, "cuda") / args.steps
+    if sdp.attn_check_device(sh) != sdp.ATTN_OK:
+        raise RuntimeError("device error in timed steps")
+    moved = w.bytes_moved(x.key_lens)
+    gbs = moved / (ms_step * 1e-3) / 1e9
+    # end to end: the cache stays resident (as in generation); q goes up, O and lse come back
+    hq = torch.from_numpy(x.q.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    hlse = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+        hlse.copy_(lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(e2.elapsed_time(e3) / args.e2e_steps, ws, "cuda")
+    peaks = measured_peaks()
+    line = {
+        "metric": "attention_decode_bandwidth", "value": gbs * ws, "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d,
+                   "bytes_per_step": moved, "l2": "cache larger than L2" if moved > 126e6 else "fits in L2"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": peaks["source"] + " copy bandwidth (MEASURED_PEAKS.json)",
+                     "kernel": "decode_partial + decode_combine"},
+        "e2e": {"value": moved * ws / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": hq.numel() * 2, "d2h_bytes_per_step": hout.numel() * 2 + hlse.numel() * 4,
+                "ms_per_step": ms_e2e},
+        "gpu_launches": 2 * args.steps,
+        "clocks": sampler.summary(),
+        "kernel_src_sha": kernel_source_sha(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -259,6 +365,10 @@ def main() -> int:
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None, help="override B (smaller cases for profiling)")
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller cases for profiling)")
+    ap.add_argument("--decode", default=None, choices=list(I.DECODE_WORKLOADS),
+                    help="time attn_decode (one query per head against a K/V cache) instead")
+    ap.add_argument("--window", type=int, default=0,
+                    help="sliding window (attn_fwd_window): query i sees keys j > i - window")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -267,10 +377,16 @@ def main() -> int:
         B = w.B if args.batch is None else args.batch
         H = w.H if args.heads is None else args.heads
         w = dataclasses.replace(w, name="%s@B%dH%d" % (w.name, B, H), B=B, H=H)
+    if args.window:
+        if w.key_len_range:
+            ap.error("--window is measured on workloads without key lengths")
+        w = dataclasses.replace(w, name="%s@window%d" % (w.name, args.window))
     ws, rank, local = dist_setup()
 
     if args.impl == "reference":
         return run_reference(args, w, ws, rank)
+    if args.decode:
+        return run_decode(args, I.DECODE_WORKLOADS[args.decode], ws, rank, local)
 
     import torch
     import torch.distributed as dist
@@ -291,7 +407,10 @@ def main() -> int:
     sh = stream.cuda_stream
 
     def step():
-        st = sdp.attn_fwd(q, k, v, out, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, kl, sh)
+        if args.window:
+            st = sdp.attn_fwd_window(q, k, v, out, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, kl, args.window, sh)
+        else:
+            st = sdp.attn_fwd(q, k, v, out, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, kl, sh)
         if st != sdp.ATTN_OK:
             raise sdp.AttnError(st)
 
@@ -328,7 +447,7 @@ def main() -> int:
     if not bool(torch.isfinite(out).all()) or not bool(torch.isfinite(lse).all()):
         raise RuntimeError("non-finite output")
     ms_step = ms_total / args.steps
-    flops = w.flops()
+    flops = window_flops(w, args.window) if args.window else w.flops()
     value = job_tflops(flops, ws, ms_step)
 
     # ------------------------------------------------ end to end (host buffers)

@@ -15,7 +15,8 @@
  *   -- hotelren.com sec. 4.1 (FlashAttention-1: tiles of Q and K/V, online
  *      softmax, the n x n score matrix is never written out).
  *
- * attn_fwd_window adds a sliding window (keys j > i - w only).
+ * attn_fwd_window adds a sliding window (keys j > i - w only); attn_decode
+ * computes one query per (batch, head) against a key/value cache.
  *
  * Mask (attn_fwd): key j is visible to query i iff j < key_lens[b] (a key-padding mask,
  * lshu.cn "Self-attention meets the compute wall", sec. 4.1 and 5.2) and,
@@ -30,6 +31,7 @@
 #ifndef SDP18_ATTN_H
 #define SDP18_ATTN_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -104,6 +106,40 @@ attn_status attn_fwd_window(const void *q, const void *k, const void *v,
                             const int32_t *key_lens, int window, attn_stream_t stream);
 
 /*
+ * attn_decode -- one new query per (batch, head) against a key/value cache.
+ *
+ *   O[b,h] = softmax(q[b,h] K[b,h,:len]^T * scale) V[b,h,:len],
+ *   lse[b,h] = ln sum_{j < len} exp(scale * q . k_j),   len = cache_lens[b]
+ *
+ * The cache is the pages' [batch, heads, seq_len, head_dim] key/value store
+ * that each generation step appends one row to (hotelren.com "AI attention:
+ * essence and evolution", sec. 3.1); the new token's own key and value are
+ * expected to be appended already, so every cached key is visible.
+ *
+ * q        : device, bf16, [B, H, d] contiguous.
+ * k_cache,
+ * v_cache  : device, bf16, [B, H, L, d] contiguous (L = allocated rows).
+ * out      : device, bf16, [B, H, d].  lse: device fp32 [B, H] or NULL.
+ * d        : 64 or 128 (else ATTN_EUNSUPPORTED); scale finite and > 0.
+ * cache_lens: device int32 [B] or NULL (all L rows hold keys); clamped to
+ *           [0, L] on the device.  len == 0 gives O = 0, lse = -inf.
+ * workspace: device scratch of at least attn_decode_workspace_size(B, H, L,
+ *           d) bytes, 16-byte aligned, owned by the caller; the call
+ *           overwrites it (no zeroing needed) and it must not be shared with
+ *           another call in flight.  Missing or too small -> ATTN_EINVAL.
+ * All tensor pointers 16-byte aligned (else ATTN_EALIGN).  B*H == 0 -> OK,
+ * nothing launched.  Asynchronous on `stream`; allocates nothing.
+ */
+attn_status attn_decode(const void *q, const void *k_cache, const void *v_cache,
+                        void *out, float *lse,
+                        int B, int H, int L, int d, float scale,
+                        const int32_t *cache_lens, void *workspace, size_t workspace_bytes,
+                        attn_stream_t stream);
+
+/* Bytes of workspace attn_decode needs for these sizes (0 for invalid sizes). */
+size_t attn_decode_workspace_size(int B, int H, int L, int d);
+
+/*
  * attn_check_device -- synchronise `stream`, then read and clear the
  * library's device error word on the current device.  Returns ATTN_EDEVICE
  * if a kernel since the last check gave up on a bounded wait (its outputs are
@@ -117,7 +153,7 @@ const char *attn_status_str(attn_status s);
 /* ABI version of this header (bumped on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 2
+#define ATTN_ABI_VERSION 3
 
 #ifdef __cplusplus
 }

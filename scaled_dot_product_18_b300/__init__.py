@@ -26,7 +26,8 @@ ATTN_ECUDA = -4
 ATTN_EDEVICE = -5
 
 # Symbols declared in include/attn.h.
-EXPORTS = ("attn_fwd", "attn_fwd_window", "attn_check_device", "attn_status_str", "attn_abi_version")
+EXPORTS = ("attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_workspace_size", "attn_check_device",
+           "attn_status_str", "attn_abi_version")
 
 _lib = None
 
@@ -50,6 +51,10 @@ def load_library():
     lib.attn_fwd.restype = i
     lib.attn_fwd_window.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, vp, i, vp]
     lib.attn_fwd_window.restype = i
+    lib.attn_decode.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, vp, vp, ctypes.c_size_t, vp]
+    lib.attn_decode.restype = i
+    lib.attn_decode_workspace_size.argtypes = [i, i, i, i]
+    lib.attn_decode_workspace_size.restype = ctypes.c_size_t
     lib.attn_check_device.argtypes = [vp]
     lib.attn_check_device.restype = i
     lib.attn_status_str.argtypes = [i]
@@ -91,6 +96,42 @@ def attn_fwd_window(q, k, v, out, lse, B: int, H: int, N: int, d: int, scale: fl
     lib = load_library()
     return lib.attn_fwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), int(B), int(H), int(N), int(d),
                                float(scale), 1 if causal else 0, _ptr(key_lens), int(window), _stream(stream))
+
+
+def attn_decode(q, k_cache, v_cache, out, lse, B: int, H: int, L: int, d: int, scale: float, cache_lens=None,
+                workspace=None, workspace_bytes: int = 0, stream=None) -> int:
+    """The C ``attn_decode``: one query per (b, h) against a [B, H, L, d] cache."""
+    lib = load_library()
+    return lib.attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), int(B), int(H), int(L),
+                           int(d), float(scale), _ptr(cache_lens), _ptr(workspace), int(workspace_bytes),
+                           _stream(stream))
+
+
+def attn_decode_workspace_size(B: int, H: int, L: int, d: int) -> int:
+    return int(load_library().attn_decode_workspace_size(int(B), int(H), int(L), int(d)))
+
+
+def decode(q, k_cache, v_cache, cache_lens=None, scale: float | None = None, stream=None, out=None, lse=None,
+           workspace=None):
+    """Convenience wrapper over ``attn_decode`` for torch tensors: q [B, H, d],
+    caches [B, H, L, d] (bf16, CUDA, contiguous).  Allocates out, lse and the
+    workspace with torch when not given; raises ``AttnError`` on failure."""
+    import torch
+    B, H, L, d = k_cache.shape
+    if out is None:
+        out = torch.empty((B, H, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    nbytes = attn_decode_workspace_size(B, H, max(L, 1), d)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    st = attn_decode(q, k_cache, v_cache, out, lse, B, H, L, d, scale, cache_lens, workspace,
+                     workspace.numel() * workspace.element_size(), stream)
+    if st != ATTN_OK:
+        raise AttnError(st, "attn_decode")
+    return out, lse
 
 
 def attn_check_device(stream=None) -> int:

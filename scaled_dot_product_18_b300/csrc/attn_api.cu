@@ -109,6 +109,59 @@ attn_status attn_fwd_window(const void *q, const void *k, const void *v, void *o
     return forward(q, k, v, out, lse, B, H, N, d, scale, causal, key_lens, window, stream);
 }
 
+size_t attn_decode_workspace_size(int B, int H, int L, int d)
+{
+    if (B <= 0 || H <= 0 || L <= 0 || (d != 64 && d != 128)) return 0;
+    const sdp18::DecodeSplit sp = sdp18::decode_split(B, H, L);
+    const size_t slots = static_cast<size_t>(B) * H * sp.splits;
+    const size_t o_bytes = (slots * d * sizeof(float) + 255) / 256 * 256;
+    return o_bytes + slots * sizeof(float);
+}
+
+attn_status attn_decode(const void *q, const void *k_cache, const void *v_cache, void *out, float *lse, int B, int H,
+                        int L, int d, float scale, const int32_t *cache_lens, void *workspace,
+                        size_t workspace_bytes, attn_stream_t stream)
+{
+    if (B < 0 || H < 0 || L < 0) return ATTN_EINVAL;
+    if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_EINVAL;
+    if (B == 0 || H == 0) return ATTN_OK;
+    if (!q || !out) return ATTN_EINVAL;
+    if (static_cast<int64_t>(B) * H > INT32_MAX / 64) return ATTN_EINVAL;
+    if (L > 0 && (!k_cache || !v_cache)) return ATTN_EINVAL;
+    const size_t need = attn_decode_workspace_size(B, H, L > 0 ? L : 1, d);
+    if (!workspace || workspace_bytes < need) return ATTN_EINVAL;
+    if (misaligned(q) || misaligned(out) || misaligned(workspace) || (L > 0 && (misaligned(k_cache) || misaligned(v_cache))))
+        return ATTN_EALIGN;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_EALIGN;
+    if (cache_lens && (reinterpret_cast<uintptr_t>(cache_lens) & 3u)) return ATTN_EALIGN;
+
+    const int Lx = L > 0 ? L : 1;  // an empty cache runs one empty split per head
+    const sdp18::DecodeSplit sp = sdp18::decode_split(B, H, Lx);
+    const size_t slots = static_cast<size_t>(B) * H * sp.splits;
+    sdp18::DecodeLaunch a{};
+    a.q = q;
+    a.k = L > 0 ? k_cache : q;  // never read when L == 0 (L_keys = 0: every split is empty)
+    a.v = L > 0 ? v_cache : q;
+    a.out = out;
+    a.lse = lse;
+    a.cache_lens = L > 0 ? cache_lens : nullptr;
+    a.part_o = static_cast<float *>(workspace);
+    a.part_lse = reinterpret_cast<float *>(static_cast<char *>(workspace) + (slots * d * sizeof(float) + 255) / 256 * 256);
+    a.B = B;
+    a.H = H;
+    a.L = Lx;
+    a.L_keys = L;
+    a.d = d;
+    a.splits = sp.splits;
+    a.chunk = sp.chunk;
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    const int rc = sdp18::attn_decode_launch(a);
+    if (rc == -2) return ATTN_EUNSUPPORTED;
+    return rc == 0 ? ATTN_OK : ATTN_ECUDA;
+}
+
 attn_status attn_check_device(attn_stream_t stream)
 {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ECUDA;

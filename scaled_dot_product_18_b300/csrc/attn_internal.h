@@ -23,6 +23,28 @@ struct AttnLaunch {
 // 0 on success, -1 on a CUDA error, -2 for an unsupported head dimension.
 int attn_fwd_launch(const AttnLaunch &a);
 
+// Decode (one query per (b, h) against a K/V cache of L rows).
+struct DecodeSplit {
+    int splits;  // cache chunks per (b, h)
+    int chunk;   // keys per chunk (a multiple of 64)
+};
+DecodeSplit decode_split(int B, int H, int L);
+
+struct DecodeLaunch {
+    const void *q, *k, *v;      // bf16 [B*H, d], [B*H, L, d], [B*H, L, d]
+    void *out;                  // bf16 [B*H, d]
+    float *lse;                 // fp32 [B*H] or nullptr
+    const int32_t *cache_lens;  // [B] or nullptr
+    float *part_o;              // fp32 [B*H, splits, d] workspace
+    float *part_lse;            // fp32 [B*H, splits] workspace
+    int B, H, L, d, splits, chunk;
+    int L_keys;  // cached rows that hold keys (L_keys <= L; L is the row stride)
+    float scale_log2;
+    cudaStream_t stream;
+};
+// 0 on success, -1 on a CUDA error, -2 for an unsupported head dimension.
+int attn_decode_launch(const DecodeLaunch &a);
+
 // Reads the device error word of the current device and clears it.
 int read_and_clear_device_error(int *value);
 

@@ -218,3 +218,45 @@ def make_inputs(w: Workload, seed: int | None = None) -> HostInputs:
     v = make_tensor_bits(s, STREAM_V, shape, w.amplitude)
     kl = make_key_lens(s, w.B, *w.key_len_range) if w.key_len_range else None
     return HostInputs(q, k, v, kl)
+
+
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    """One query per (batch, head) against a [B, H, L, d] key/value cache, the
+    cache layout of the pages' KV-cache section (hotelren.com "AI attention:
+    essence and evolution", sec. 3.1).  cache_len_range: inclusive [lo, hi]
+    drawn per batch element, or None for full caches."""
+    name: str
+    B: int
+    H: int
+    L: int
+    d: int
+    cache_len_range: tuple[int, int] | None = None
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(np.sqrt(self.d))
+
+    def bytes_moved(self, cache_lens=None) -> int:
+        """K and V rows read for the visible keys, plus q, O (bf16) and lse."""
+        rows = self.B * self.L if cache_lens is None else int(np.sum(np.clip(cache_lens, 0, self.L)))
+        return rows * self.H * self.d * 2 * 2 + 2 * self.B * self.H * self.d * 2 + self.B * self.H * 4
+
+
+# Llama-3-8B-like heads (32 x 128) at the pages' 2048-token input length, and
+# the long-context length of the 16K example.
+DECODE_WORKLOADS = {
+    "decode_b16h32l2048d128": DecodeWorkload("decode_b16h32l2048d128", 16, 32, 2048, 128),
+    "decode_b4h32l16384d128": DecodeWorkload("decode_b4h32l16384d128", 4, 32, 16384, 128),
+}
+
+
+def make_decode_inputs(w: DecodeWorkload, seed: int | None = None) -> HostInputs:
+    """q [B, H, d], caches [B, H, L, d] (bf16 bits), cache_lens [B] or None."""
+    s = w.seed if seed is None else seed
+    q = make_tensor_bits(s, STREAM_Q, (w.B, w.H, w.d))
+    k = make_tensor_bits(s, STREAM_K, (w.B, w.H, w.L, w.d))
+    v = make_tensor_bits(s, STREAM_V, (w.B, w.H, w.L, w.d))
+    cl = make_key_lens(s, w.B, *w.cache_len_range) if w.cache_len_range else None
+    return HostInputs(q, k, v, cl)

@@ -29,14 +29,15 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert {"attn_fwd", "attn_fwd_window", "attn_check_device", "attn_status_str", "attn_abi_version"} <= names
+    assert {"attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_workspace_size", "attn_check_device",
+            "attn_status_str", "attn_abi_version"} <= names
     assert names == set(sdp.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
 
 
 def test_abi_version_and_status_strings(lib):
-    assert sdp.attn_abi_version() == 2
+    assert sdp.attn_abi_version() == 3
     for code in (0, -1, -2, -3, -4, -5):
         assert sdp.attn_status_str(code).startswith("ATTN_")
     assert sdp.attn_status_str(7) == "unknown attn_status"
@@ -90,6 +91,40 @@ def test_window_rejections(lib, window, want):
 
 def test_window_empty_problem_is_ok(lib):
     assert lib.attn_fwd_window(None, None, None, None, None, 0, 3, 5, 64, 0.125, 1, None, 7, None) == sdp.ATTN_OK
+
+
+def test_decode_workspace_size(lib):
+    n = sdp.attn_decode_workspace_size(4, 32, 16384, 128)
+    assert n > 0 and n % 4 == 0
+    assert sdp.attn_decode_workspace_size(4, 32, 16384, 96) == 0
+    assert sdp.attn_decode_workspace_size(0, 32, 16384, 128) == 0
+    # more splits per head when there are few heads, never more than one per 256 keys
+    assert sdp.attn_decode_workspace_size(1, 1, 256, 64) == (256 + 4)  # one split: 64 floats (256 B) + 1 lse
+    assert sdp.attn_decode_workspace_size(1, 1, 100000, 128) > sdp.attn_decode_workspace_size(64, 1, 100000, 128) / 64
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(d=96), sdp.ATTN_EUNSUPPORTED),
+    (dict(B=-1), sdp.ATTN_EINVAL),
+    (dict(L=-1), sdp.ATTN_EINVAL),
+    (dict(scale=0.0), sdp.ATTN_EINVAL),
+    (dict(q=None), sdp.ATTN_EINVAL),
+    (dict(out=None), sdp.ATTN_EINVAL),
+    (dict(k=None), sdp.ATTN_EINVAL),
+    (dict(ws=None), sdp.ATTN_EINVAL),
+    (dict(ws_bytes=16), sdp.ATTN_EINVAL),
+    (dict(q=P + 8), sdp.ATTN_EALIGN),
+    (dict(v=P + 4), sdp.ATTN_EALIGN),
+    (dict(ws=P + 8), sdp.ATTN_EALIGN),
+    (dict(B=0, q=None, out=None, ws=None), sdp.ATTN_OK),
+])
+def test_decode_host_side_rejections(lib, args, want):
+    a = dict(q=P, k=P, v=P, out=P, lse=None, B=2, H=3, L=1000, d=128, scale=0.1, cl=None, ws=P,
+             ws_bytes=1 << 30, stream=None)
+    a.update(args)
+    st = lib.attn_decode(a["q"], a["k"], a["v"], a["out"], a["lse"], a["B"], a["H"], a["L"], a["d"], a["scale"],
+                         a["cl"], a["ws"], a["ws_bytes"], a["stream"])
+    assert st == want, (args, st)
 
 
 def test_binding_raises_without_library(tmp_path, monkeypatch):

@@ -348,3 +348,41 @@ def _all_pins_pass(fn):
 def test_pins_catch_planted_mistakes(kind):
     assert _all_pins_pass(_mutant("none"))
     assert not _all_pins_pass(_mutant(kind)), kind
+
+
+# --- one query against a key/value cache (decode) -------------------------------
+
+def test_decode_rows_match_literal_square_problem():
+    # A decode query (Nq = 1) seeing keys 0..cache_len-1 is row i of a square
+    # non-causal problem whose key lengths are cache_len: the literal
+    # materialised-matrix oracle computes that row independently.
+    r = np.random.default_rng(41)
+    B, H, L, d = 2, 3, 17, 5
+    k = r.standard_normal((B, H, L, d))
+    v = r.standard_normal((B, H, L, d))
+    q1 = r.standard_normal((B, H, 1, d))
+    cl = np.array([11, 17], dtype=np.int32)
+    O1, l1 = oracle.attention_rows(q1, k, v, 0.45, False, cl, threads=2)
+    for i in (0, 7, 16):
+        Q = r.standard_normal((B, H, L, d))
+        Q[:, :, i] = q1[:, :, 0]
+        O2, l2, _ = oracle.attention_literal(Q, k, v, 0.45, False, cl)
+        np.testing.assert_allclose(O1[:, :, 0], O2[:, :, i], atol=1e-12)
+        np.testing.assert_allclose(l1[:, :, 0], l2[:, :, i], atol=1e-12)
+
+
+def test_decode_zero_query_and_empty_cache():
+    r = np.random.default_rng(42)
+    B, H, L, d = 3, 2, 12, 4
+    k = r.standard_normal((B, H, L, d))
+    v = r.standard_normal((B, H, L, d))
+    q1 = np.zeros((B, H, 1, d))
+    cl = np.array([5, 0, 12], dtype=np.int32)
+    O, lse = oracle.attention_rows(q1, k, v, 0.7, False, cl, threads=2)
+    for b in range(B):
+        n = int(cl[b])
+        if n == 0:
+            assert np.all(O[b] == 0.0) and np.all(np.isneginf(lse[b]))
+        else:
+            np.testing.assert_allclose(O[b, :, 0], v[b, :, :n].mean(axis=1), atol=1e-12)
+            np.testing.assert_allclose(lse[b, :, 0], math.log(n), atol=1e-12)
