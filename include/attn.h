@@ -47,7 +47,8 @@ typedef enum {
     ATTN_EUNSUPPORTED = -2,/* head dimension d other than 64 or 128 */
     ATTN_EALIGN = -3,      /* a tensor pointer not 16-byte aligned (TMA requirement) */
     ATTN_ECUDA = -4,       /* CUDA runtime/driver error (launch, tensor-map encode, no sm_103a device) */
-    ATTN_EDEVICE = -5      /* the kernel reported an error (a bounded wait ran out) */
+    ATTN_EDEVICE = -5,     /* the kernel reported an error (a bounded wait ran out) */
+    ATTN_ETOOLARGE = -6    /* the problem needs more scratch than attn_decode_noalloc's fixed area */
 } attn_status;
 
 /*
@@ -138,6 +139,33 @@ attn_status attn_decode(const void *q, const void *k_cache, const void *v_cache,
 
 /* Bytes of workspace attn_decode needs for these sizes (0 for invalid sizes). */
 size_t attn_decode_workspace_size(int B, int H, int L, int d);
+
+/*
+ * attn_decode_noalloc -- attn_decode for callers that cannot allocate.
+ *
+ * The pages have no counterpart; this entry point exists for callers that
+ * may not call cudaMalloc once they are running (a serving or real-time loop
+ * whose memory was fixed at start-up, a host program that lends this library
+ * a stream but no allocator, or a step loop that cannot afford cudaMalloc's
+ * implicit device synchronisation).  Same arguments, results and errors as
+ * attn_decode, without the workspace: the split partials go to one fixed
+ * 8 MiB array of device memory that the library holds on every device that
+ * loads it, for the life of the process.  The call allocates nothing.
+ *
+ * - Problems whose attn_decode_workspace_size exceeds 8 MiB return
+ *   ATTN_ETOOLARGE before anything is launched (about 16,000 (batch, head)
+ *   pairs at d = 128; use attn_decode with a caller workspace beyond that).
+ * - The first call on each device looks up that device's array address
+ *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ * - Every call on a device shares the one array and leaves its partials in
+ *   it.  Nothing in it needs clearing (each call writes every slot it reads),
+ *   but calls that overlap on the GPU -- on different streams, or from
+ *   different host threads without ordering -- race on it: serialise them.
+ */
+attn_status attn_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                void *out, float *lse,
+                                int B, int H, int L, int d, float scale,
+                                const int32_t *cache_lens, attn_stream_t stream);
 
 /*
  * attn_check_device -- synchronise `stream`, then read and clear the

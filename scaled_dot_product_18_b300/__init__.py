@@ -24,10 +24,11 @@ ATTN_EUNSUPPORTED = -2
 ATTN_EALIGN = -3
 ATTN_ECUDA = -4
 ATTN_EDEVICE = -5
+ATTN_ETOOLARGE = -6
 
 # Symbols declared in include/attn.h.
-EXPORTS = ("attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_workspace_size", "attn_check_device",
-           "attn_status_str", "attn_abi_version")
+EXPORTS = ("attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_workspace_size", "attn_decode_noalloc",
+           "attn_check_device", "attn_status_str", "attn_abi_version")
 
 _lib = None
 
@@ -55,6 +56,8 @@ def load_library():
     lib.attn_decode.restype = i
     lib.attn_decode_workspace_size.argtypes = [i, i, i, i]
     lib.attn_decode_workspace_size.restype = ctypes.c_size_t
+    lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, vp, vp]
+    lib.attn_decode_noalloc.restype = i
     lib.attn_check_device.argtypes = [vp]
     lib.attn_check_device.restype = i
     lib.attn_status_str.argtypes = [i]
@@ -105,6 +108,15 @@ def attn_decode(q, k_cache, v_cache, out, lse, B: int, H: int, L: int, d: int, s
     return lib.attn_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), int(B), int(H), int(L),
                            int(d), float(scale), _ptr(cache_lens), _ptr(workspace), int(workspace_bytes),
                            _stream(stream))
+
+
+def attn_decode_noalloc(q, k_cache, v_cache, out, lse, B: int, H: int, L: int, d: int, scale: float,
+                        cache_lens=None, stream=None) -> int:
+    """The C ``attn_decode_noalloc``: ``attn_decode`` on the library's fixed
+    per-device scratch array, for callers that cannot allocate."""
+    lib = load_library()
+    return lib.attn_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), _ptr(lse), int(B), int(H),
+                                   int(L), int(d), float(scale), _ptr(cache_lens), _stream(stream))
 
 
 def attn_decode_workspace_size(B: int, H: int, L: int, d: int) -> int:

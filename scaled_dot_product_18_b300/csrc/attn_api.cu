@@ -179,6 +179,7 @@ const char *attn_status_str(attn_status s)
     case ATTN_EALIGN: return "ATTN_EALIGN: tensor pointer not 16-byte aligned";
     case ATTN_ECUDA: return "ATTN_ECUDA: CUDA error";
     case ATTN_EDEVICE: return "ATTN_EDEVICE: kernel gave up on a bounded wait";
+    case ATTN_ETOOLARGE: return "ATTN_ETOOLARGE: problem exceeds the fixed scratch area of attn_decode_noalloc";
     }
     return "unknown attn_status";
 }

@@ -25,7 +25,9 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
+#include "attn.h"
 #include "attn_internal.h"
 
 namespace sdp18 {
@@ -224,3 +226,62 @@ int attn_decode_launch(const DecodeLaunch &a)
 }
 
 }  // namespace sdp18
+
+// ---------------------------------------------------------------------------
+// attn_decode_noalloc: attn_decode on a workspace the library owns.
+//
+// Some callers cannot allocate device memory once they are running: a serving
+// or real-time loop that fixed its memory budget at start-up, a host
+// application that hands this library a stream but no allocator, or code that
+// must not pay cudaMalloc's implicit device synchronisation on every step.
+// For them the split partials live in one fixed array of device memory that
+// is part of the loaded library.  Its device address is looked up once per
+// device (the first call on that device does it), and each call then passes
+// that address as the workspace of attn_decode.
+namespace sdp18 {
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB per device
+constexpr int kMaxDevices = 64;
+
+// Lives on every device that loads the library, for as long as the process
+// runs.  Host code may not use this name as a pointer: on the host it only
+// identifies the symbol, so its device address is fetched below.
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+// Device address of g_decode_scratch on the current device, or nullptr.
+void *static_scratch()
+{
+    static std::mutex mu;
+    static void *addr[kMaxDevices] = {};
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
+}  // namespace
+}  // namespace sdp18
+
+extern "C" attn_status attn_decode_noalloc(const void *q, const void *k_cache, const void *v_cache, void *out,
+                                           float *lse, int B, int H, int L, int d, float scale,
+                                           const int32_t *cache_lens, attn_stream_t stream)
+{
+    if (B < 0 || H < 0 || L < 0) return ATTN_EINVAL;
+    if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
+    if (B == 0 || H == 0) return ATTN_OK;
+    const size_t need = attn_decode_workspace_size(B, H, L > 0 ? L : 1, d);
+    if (need == 0) return ATTN_EINVAL;
+    if (need > sdp18::kStaticScratchBytes) return ATTN_ETOOLARGE;
+    void *ws = sdp18::static_scratch();
+    if (ws == nullptr) return ATTN_ECUDA;
+    // Nothing in the workspace needs to start at zero: every split writes all
+    // of its partial slots before the combine kernel reads them.
+    return attn_decode(q, k_cache, v_cache, out, lse, B, H, L, d, scale, cache_lens, ws, sdp18::kStaticScratchBytes,
+                       stream);
+}
