@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kDecThreads)
 {
     constexpr int kSeg = D / 8;                 // threads per key row
     constexpr int kRows = kDecThreads / kSeg;   // key rows per step
-    constexpr int kUnroll = 4;                  // steps with loads in flight
+    constexpr int kUnroll = 8;                  // steps with loads in flight
     __shared__ float s_o[kRows][D];
     __shared__ float s_m[kRows], s_l[kRows];
 
@@ -204,9 +204,9 @@ int launch_decode(const DecodeLaunch &a)
 DecodeSplit decode_split(int B, int H, int L)
 {
     // Enough CTAs for every SM to keep many 16-byte loads in flight: about
-    // eight per SM, each split at least 256 keys, chunks a multiple of 64.
+    // sixteen per SM, each split at least 256 keys, chunks a multiple of 64.
     const int64_t heads = static_cast<int64_t>(B) * H;
-    const int64_t target = 148 * 8;
+    const int64_t target = 148 * 16;
     int64_t splits = (target + heads - 1) / heads;
     const int64_t max_splits = (static_cast<int64_t>(L) + 255) / 256;
     if (splits > max_splits) splits = max_splits;

@@ -112,7 +112,10 @@ __device__ __forceinline__ KeyRange key_range(int q0t, int N, int kv_len, int ca
     return {lo / kBN, (kv_end + kBN - 1) / kBN};
 }
 
-template <int D>
+// kWindow = false compiles the plain causal / key-length kernel; true adds
+// the sliding-window ranges, the lower-edge mask and the guards for rows that
+// have not seen a visible key yet.
+template <int D, bool kWindow>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -139,6 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = bh / H;
     int kv_len = N;
     if (key_lens != nullptr) kv_len = min(max(key_lens[b], 0), N);
+    if constexpr (!kWindow) window = 0;
     const KeyRange kr[2] = {key_range(q0, N, kv_len, causal, window),
                             key_range(q0 + kBM, N, kv_len, causal, window)};
     const int n0 = kr[0].count(), n1 = kr[1].count();
@@ -260,39 +264,69 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (active(t, 0)) issue_s(t, 0);
                 mma_commit_one(bar(L::kBarEmpty + 0));
             }
-            for (int j = 0; j < n_max && ok; ++j) {
-                const int v_item = 2 * j + 1, k_item = 2 * j + 2;
-                const int vs = v_item % L::kNumSlots, ks = k_item % L::kNumSlots;
-                ok = wait_full(v_item, 4);
-                const bool k_next = j + 1 < n_max;  // K_{j+1} is streamed: consume it below
-                bool k_ready = false;
-#pragma unroll
-                for (int t = 0; t < 2; ++t) {
-                    if (!ok) break;
-                    if (active(t, j)) {
-                        const int jj = j - f_t[t];
-                        ok = wait_warp(bar(L::kBarPFull + t), jj & 1, 5 + t);
+            if constexpr (!kWindow) {
+                // Both tiles start at key tile 0; tile 1 may run one tile longer.
+                for (int j = 0; j < n_max && ok; ++j) {
+                    const int v_item = 2 * j + 1, k_item = 2 * j + 2;
+                    const int vs = v_item % L::kNumSlots, ks = k_item % L::kNumSlots;
+                    ok = wait_full(v_item, 4);
+                    bool k_ready = false;
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (j >= n_t[t]) continue;
+                        ok = wait_warp(bar(L::kBarPFull + t), j & 1, 5 + t);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_pv(t, vs, jj > 0);
-                        if (jj + 1 == n_t[t]) mma_commit_one(bar(L::kBarODone + t));
-                    }
-                    if (k_next && active(t, j + 1)) {
-                        if (!k_ready) {
-                            ok = wait_full(k_item, 7);
-                            if (!ok) break;
-                            k_ready = true;
+                        issue_pv(t, vs, j > 0);
+                        if (j + 1 < n_t[t]) {
+                            if (!k_ready) {
+                                ok = wait_full(k_item, 7);
+                                if (!ok) break;
+                                k_ready = true;
+                            }
+                            issue_s(t, ks);
+                        } else {
+                            mma_commit_one(bar(L::kBarODone + t));
                         }
-                        issue_s(t, ks);
                     }
+                    if (!ok) break;
+                    mma_commit_one(bar(L::kBarEmpty + vs));
+                    if (k_ready) mma_commit_one(bar(L::kBarEmpty + ks));
                 }
-                if (ok && k_next && !k_ready) {
-                    ok = wait_full(k_item, 7);  // streamed but used by neither tile
-                    k_ready = ok;
+            } else {
+                for (int j = 0; j < n_max && ok; ++j) {
+                    const int v_item = 2 * j + 1, k_item = 2 * j + 2;
+                    const int vs = v_item % L::kNumSlots, ks = k_item % L::kNumSlots;
+                    ok = wait_full(v_item, 4);
+                    const bool k_next = j + 1 < n_max;  // K_{j+1} is streamed: consume it below
+                    bool k_ready = false;
+    #pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        if (!ok) break;
+                        if (active(t, j)) {
+                            const int jj = j - f_t[t];
+                            ok = wait_warp(bar(L::kBarPFull + t), jj & 1, 5 + t);
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_pv(t, vs, jj > 0);
+                            if (jj + 1 == n_t[t]) mma_commit_one(bar(L::kBarODone + t));
+                        }
+                        if (k_next && active(t, j + 1)) {
+                            if (!k_ready) {
+                                ok = wait_full(k_item, 7);
+                                if (!ok) break;
+                                k_ready = true;
+                            }
+                            issue_s(t, ks);
+                        }
+                    }
+                    if (ok && k_next && !k_ready) {
+                        ok = wait_full(k_item, 7);  // streamed but used by neither tile
+                        k_ready = ok;
+                    }
+                    if (!ok) break;
+                    mma_commit_one(bar(L::kBarEmpty + vs));
+                    if (k_ready) mma_commit_one(bar(L::kBarEmpty + ks));
                 }
-                if (!ok) break;
-                mma_commit_one(bar(L::kBarEmpty + vs));
-                if (k_ready) mma_commit_one(bar(L::kBarEmpty + ks));
             }
             // Every MMA must be finished before TMEM is released.
             mma_commit_one(bar(L::kBarDrain));
@@ -332,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 lim = kv_len - j * kBN;
                 if (causal) lim = min(lim, q_abs - j * kBN + 1);
             }
-            const bool lower = window > 0 && j * kBN < q0t + kBM - window;  // some row's window starts here
+            const bool lower = kWindow && j * kBN < q0t + kBM - window;  // some row's window starts here
             const int lim_lo = q_abs - window + 1 - j * kBN;
             // 64 score columns from TMEM (two 32-column loads), masked.
             auto load64 = [&](int c0, uint32_t (&ra)[32], uint32_t (&rb)[32]) {
@@ -378,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // A row that has seen no visible key yet keeps m = -inf; its
             // scores are all -inf too, so any finite shift gives P = 0.
-            const float m_use = m == -INFINITY ? 0.f : m;
+            const float m_use = (kWindow && m == -INFINITY) ? 0.f : m;
             const float2 nm2 = make_float2(-m_use, -m_use);
 
             // O_t += P_t V_{j-1} is complete (the S_t commit covers it), so O_t
@@ -444,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (ok) {
                 // Rows with no visible key (l_o = 0) get O = 0 and lse = -inf.
-                const float inv_l = have && l_o > 0.f ? 1.f / l_o : 0.f;
+                const float inv_l = have && (!kWindow || l_o > 0.f) ? 1.f / l_o : 0.f;
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
@@ -467,7 +501,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (lse != nullptr && q_abs < N) {
-                    const float v = have && l > 0.f ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
+                    const float v =
+                        have && (!kWindow || l > 0.f) ? (m + log2f(l)) * 0.69314718055994531f : -INFINITY;
                     lse[static_cast<int64_t>(bh) * N + q_abs] = v;
                 }
             }
@@ -489,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int D>
+template <int D, bool kWindow>
 int launch(const AttnLaunch &a)
 {
     using L = Smem<D>;
@@ -497,15 +532,15 @@ int launch(const AttnLaunch &a)
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (configured_device != dev) {
-        if (cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(attn_fwd_kernel<D, kWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 L::kAlloc) != cudaSuccess)
             return -1;
         configured_device = dev;
     }
     const int num_q_pairs = (a.N + kRowsPerCta - 1) / kRowsPerCta;
     const int num_bh = a.B * a.H;
     const unsigned grid = static_cast<unsigned>(num_q_pairs) * static_cast<unsigned>(num_bh);
-    attn_fwd_kernel<D><<<grid, kThreads, L::kAlloc, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, a.lse,
+    attn_fwd_kernel<D, kWindow><<<grid, kThreads, L::kAlloc, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, a.lse,
                                                                  a.key_lens, a.H, a.N, num_q_pairs, num_bh,
                                                                  a.scale_log2, a.causal, a.window);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
@@ -515,8 +550,9 @@ int launch(const AttnLaunch &a)
 
 int attn_fwd_launch(const AttnLaunch &a)
 {
-    if (a.d == 64) return launch<64>(a);
-    if (a.d == 128) return launch<128>(a);
+    const bool w = a.window > 0;
+    if (a.d == 64) return w ? launch<64, true>(a) : launch<64, false>(a);
+    if (a.d == 128) return w ? launch<128, true>(a) : launch<128, false>(a);
     return -2;
 }
 
