@@ -34,44 +34,47 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 3-D view [B*H][N][d] of a bf16 tensor, box = 64 head-dim columns x 128 rows
-// x 1 head, 128-byte swizzle (one box row = 128 bytes).  Rows past N read as
-// zeros and are clipped on store, so ragged N needs no padding.
-bool make_map(CUtensorMap *m, const void *base, int BH, int N, int d)
+// Element strides of the rows, heads and batches of a bf16 [.., d] tensor.
+struct Strides {
+    int64_t row, head, batch;
+};
+
+// 4-D view {d, N, H, B} of a bf16 tensor with the given element strides,
+// box = 64 head-dim columns x 128 rows x 1 head x 1 batch, 128-byte swizzle
+// (one box row = 128 bytes).  Rows past N read as zeros and are clipped on
+// store, so ragged N needs no padding.
+bool make_map(CUtensorMap *m, const void *base, int B, int H, int N, int d, Strides st)
 {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.row) * 2, static_cast<cuuint64_t>(st.head) * 2,
+                                   static_cast<cuuint64_t>(st.batch) * 2};
+    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Contiguous [B, H, N, d].
+Strides bhnd(int H, int N, int d)
+{
+    return {d, static_cast<int64_t>(N) * d, static_cast<int64_t>(H) * N * d};
+}
+
 bool misaligned(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
-attn_status forward(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N, int d,
-                    float scale, int causal, const int32_t *key_lens, int window, attn_stream_t stream)
+// Launch on Q/K/V/O with the given layouts (validated by the callers).
+attn_status launch_forward(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N,
+                           int d, float scale, int causal, const int32_t *key_lens, int window, Strides in_st,
+                           Strides out_st, attn_stream_t stream)
 {
-    if (B < 0 || H < 0 || N < 0 || window < 0) return ATTN_EINVAL;
-    if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
-    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_EINVAL;
-    if (B == 0 || H == 0 || N == 0) return ATTN_OK;
-    if (!q || !k || !v || !out) return ATTN_EINVAL;
-    const int64_t bh = static_cast<int64_t>(B) * H;
-    const int64_t q_tiles = (static_cast<int64_t>(N) + 127) / 128;
-    if (bh > INT32_MAX || q_tiles * bh > INT32_MAX) return ATTN_EINVAL;
-    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out)) return ATTN_EALIGN;
-    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_EALIGN;
-    if (key_lens && (reinterpret_cast<uintptr_t>(key_lens) & 3u)) return ATTN_EALIGN;
-
     CUtensorMap tq, tk, tv, to;
-    if (!make_map(&tq, q, static_cast<int>(bh), N, d) || !make_map(&tk, k, static_cast<int>(bh), N, d) ||
-        !make_map(&tv, v, static_cast<int>(bh), N, d) || !make_map(&to, out, static_cast<int>(bh), N, d))
+    if (!make_map(&tq, q, B, H, N, d, in_st) || !make_map(&tk, k, B, H, N, d, in_st) ||
+        !make_map(&tv, v, B, H, N, d, in_st) || !make_map(&to, out, B, H, N, d, out_st))
         return ATTN_ECUDA;
-
     sdp18::AttnLaunch a{};
     a.tm_q = &tq;
     a.tm_k = &tk;
@@ -90,6 +93,25 @@ attn_status forward(const void *q, const void *k, const void *v, void *out, floa
     const int rc = sdp18::attn_fwd_launch(a);
     if (rc == -2) return ATTN_EUNSUPPORTED;
     return rc == 0 ? ATTN_OK : ATTN_ECUDA;
+}
+
+attn_status forward(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N, int d,
+                    float scale, int causal, const int32_t *key_lens, int window, attn_stream_t stream)
+{
+    if (B < 0 || H < 0 || N < 0 || window < 0) return ATTN_EINVAL;
+    if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_EINVAL;
+    if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+    if (!q || !k || !v || !out) return ATTN_EINVAL;
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    const int64_t q_tiles = (static_cast<int64_t>(N) + 127) / 128;
+    if (bh > INT32_MAX || q_tiles * bh > INT32_MAX) return ATTN_EINVAL;
+    if (misaligned(q) || misaligned(k) || misaligned(v) || misaligned(out)) return ATTN_EALIGN;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_EALIGN;
+    if (key_lens && (reinterpret_cast<uintptr_t>(key_lens) & 3u)) return ATTN_EALIGN;
+
+    return launch_forward(q, k, v, out, lse, B, H, N, d, scale, causal, key_lens, window, bhnd(H, N, d),
+                          bhnd(H, N, d), stream);
 }
 
 }  // namespace

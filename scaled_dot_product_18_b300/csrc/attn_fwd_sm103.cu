@@ -33,6 +33,11 @@
 // "S_t(j+1) ready" also covers O_t += P_t V_j: a softmax warp that holds
 // S_t(j+1) may rescale O_t in place, no MMA is writing it.
 //
+// Q, K, V and O are addressed through 4-D tensor maps {d, N, H, B} with
+// arbitrary row, head and batch strides, so the heads may sit in [B, H, N, d]
+// tensors or interleaved in [B, N, H, d] rows (the output of a fused QKV
+// projection) without a transpose.
+//
 // Memory layout (all 128-byte swizzled, 1024-byte aligned tiles):
 //   Q tile t : d/64 column blocks of [128 rows x 64 bf16]; reused to stage O_t
 //   K/V ring : NSLOT slots of d/64 blocks of [128 keys x 64 bf16]
@@ -140,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qp = num_q_pairs - 1 - static_cast<int>(blockIdx.x / num_bh);
     const int q0 = qp * kRowsPerCta;
     const int b = bh / H;
+    const int h = bh % H;
     int kv_len = N;
     if (key_lens != nullptr) kv_len = min(max(key_lens[b], 0), N);
     if constexpr (!kWindow) window = 0;
@@ -193,8 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; t < 2; ++t)
                 if ((t == 0 ? n0 : n1) > 0)
                     for (int cb = 0; cb < D / 64; ++cb)
-                        tma_load_3d_one(sQ(t) + cb * kBM * 128, &tm_q, bar(L::kBarQFull), cb * 64, q0 + t * kBM,
-                                        bh);
+                        tma_load_4d_one(sQ(t) + cb * kBM * 128, &tm_q, bar(L::kBarQFull), cb * 64, q0 + t * kBM,
+                                        h, b);
             int issued = 0;
             for (int item = 0; item < 2 * n_max; ++item) {
                 const int s = item % L::kNumSlots;
@@ -204,8 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dst = sRing + s * L::kKVBytes;
                 mbar_arrive_expect_tx_one(bar(L::kBarFull + s), L::kKVBytes);
                 for (int cb = 0; cb < D / 64; ++cb)
-                    tma_load_3d_one(dst + cb * kBN * 128, map, bar(L::kBarFull + s), cb * 64,
-                                    (j_begin + (item >> 1)) * kBN, bh);
+                    tma_load_4d_one(dst + cb * kBN * 128, map, bar(L::kBarFull + s), cb * 64,
+                                    (j_begin + (item >> 1)) * kBN, h, b);
                 ++issued;
             }
             // Copies must have landed before the CTA's shared memory goes away.
@@ -511,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         named_bar_sync(1 + t, 4 * 32);
         if (row == 0 && q0t < N && !*abort_flag) {
-            for (int cb = 0; cb < D / 64; ++cb) tma_store_3d(&tm_o, sO + cb * kBM * 128, cb * 64, q0t, bh);
+            for (int cb = 0; cb < D / 64; ++cb) tma_store_4d(&tm_o, sO + cb * kBM * 128, cb * 64, q0t, h, b);
             tma_store_commit();
             tma_store_wait_all();
         }
