@@ -155,3 +155,42 @@ def attention_literal(q, k, v, scale: float, causal: bool, key_lens=None, window
     with np.errstate(divide="ignore"):
         lse = np.where(empty, -np.inf, m_safe + np.log(np.where(empty, 1.0, l)))[..., 0]
     return O, lse, P
+
+
+def round_bf16(x) -> np.ndarray:
+    """Round float64 values to the nearest bfloat16 (ties to even), returned
+    as float64.  Done on the float64 bit pattern (one rounding): keep the
+    sign, the 11 exponent bits and the top 7 fraction bits.  Finite values
+    in the normal float32 range only (true for every tensor it sees here)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    bits = x.view(np.uint64)
+    keep = np.uint64(45)  # 52 - 7 fraction bits dropped
+    half = np.uint64(1) << (keep - np.uint64(1))
+    lsb = (bits >> keep) & np.uint64(1)
+    r = (bits + (half - np.uint64(1)) + lsb) & ~((np.uint64(1) << keep) - np.uint64(1))
+    return r.view(np.float64)
+
+
+def mha_block(x, w_qkv, w_o, H: int, causal: bool, key_lens=None, threads: int | None = None):
+    """Multi-head self-attention block without biases (cnnetsun.cn
+    "Transformer QKV bottlenecks on long sequences", sec. 2, MinimalSelfAttention:
+    Q/K/V projections, split into heads, scaled dot-product attention, merge
+    heads, output projection; qqiyuan.cn's variant fuses the three projections
+    into one [E, 3E] matrix, as here).
+
+    x: [B, N, E]; w_qkv: [E, 3E] with Q, K, V columns in that order; w_o:
+    [E, E].  Q/K/V and the merged attention output are bf16 tensors in the
+    method (rounded to nearest even here, at the same two points); everything
+    else is float64.  Returns (out [B, N, E], lse [B, H, N]).
+    """
+    x, w_qkv, w_o = _as_f64(x), _as_f64(w_qkv), _as_f64(w_o)
+    B, N, E = x.shape
+    d = E // H
+    qkv = round_bf16(np.matmul(x, w_qkv))                        # [B, N, 3E]
+    heads = lambda t: t.reshape(B, N, H, d).transpose(0, 2, 1, 3)  # noqa: E731  [B, H, N, d]
+    q = np.ascontiguousarray(heads(qkv[..., :E]))
+    k = np.ascontiguousarray(heads(qkv[..., E:2 * E]))
+    v = np.ascontiguousarray(heads(qkv[..., 2 * E:]))
+    O, lse = attention_rows(q, k, v, 1.0 / np.sqrt(d), causal, key_lens, threads=threads)
+    attn = round_bf16(O.transpose(0, 2, 1, 3).reshape(B, N, E))  # merge heads
+    return np.matmul(attn, w_o), lse

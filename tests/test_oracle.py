@@ -386,3 +386,72 @@ def test_decode_zero_query_and_empty_cache():
         else:
             np.testing.assert_allclose(O[b, :, 0], v[b, :, :n].mean(axis=1), atol=1e-12)
             np.testing.assert_allclose(lse[b, :, 0], math.log(n), atol=1e-12)
+
+
+# --- multi-head block (projections + attention + output projection) -------------
+
+def _bf16_grid(r, shape, scale=1.0):
+    # values that are exact in bfloat16, so rounding does not blur the pins
+    return oracle.round_bf16(scale * r.standard_normal(shape))
+
+
+def test_round_bf16_matches_known_values():
+    vals = np.array([1.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -2.5, 3.0e-3, 1.0 + 2 ** -9])
+    want = np.array([1.0, 1.0, 1.0 + 2 ** -6, -2.5, 0.0030059814453125, 1.0])
+    np.testing.assert_array_equal(oracle.round_bf16(vals), want)
+    x = np.random.default_rng(3).standard_normal(1000)
+    r = oracle.round_bf16(x)
+    assert np.all(np.abs(r - x) <= np.abs(x) * 2.0 ** -8)
+    assert np.array_equal(oracle.round_bf16(r), r)
+
+
+def test_mha_block_brute_force():
+    # Element by element from the definition, with plain loops.
+    r = np.random.default_rng(51)
+    B, N, E, H = 2, 5, 4, 2
+    d = E // H
+    x = _bf16_grid(r, (B, N, E))
+    wqkv = _bf16_grid(r, (E, 3 * E), 0.5)
+    wo = _bf16_grid(r, (E, E), 0.5)
+    kl = np.array([3, 5], dtype=np.int32)
+    for causal in (False, True):
+        out, lse = oracle.mha_block(x, wqkv, wo, H, causal, kl, threads=1)
+        for b in range(B):
+            proj = np.zeros((N, 3 * E))
+            for n in range(N):
+                for c in range(3 * E):
+                    proj[n, c] = sum(x[b, n, e] * wqkv[e, c] for e in range(E))
+            proj = oracle.round_bf16(proj)
+            merged = np.zeros((N, E))
+            for h in range(H):
+                for i in range(N):
+                    vis = [j for j in range(N) if j < kl[b] and (not causal or j <= i)]
+                    s = [sum(proj[i, h * d + t] * proj[j, E + h * d + t] for t in range(d)) / math.sqrt(d) for j in vis]
+                    m = max(s)
+                    w = [math.exp(z - m) for z in s]
+                    tot = sum(w)
+                    for t in range(d):
+                        merged[i, h * d + t] = sum(wj * proj[j, 2 * E + h * d + t] for wj, j in zip(w, vis)) / tot
+                    assert abs(lse[b, h, i] - (m + math.log(tot))) < 1e-12
+            merged = oracle.round_bf16(merged)
+            want = np.array([[sum(merged[n, e] * wo[e, c] for e in range(E)) for c in range(E)] for n in range(N)])
+            np.testing.assert_allclose(out[b], want, atol=1e-12)
+
+
+def test_mha_block_head_permutation_invariance():
+    # Relabelling heads consistently (Q/K/V column blocks and the rows of the
+    # output projection) leaves the block's output unchanged.
+    r = np.random.default_rng(52)
+    B, N, E, H = 1, 7, 8, 4
+    d = E // H
+    x = _bf16_grid(r, (B, N, E))
+    wqkv = _bf16_grid(r, (E, 3 * E), 0.4)
+    wo = _bf16_grid(r, (E, E), 0.4)
+    perm = np.array([2, 0, 3, 1])
+    cols = np.concatenate([np.arange(h * d, (h + 1) * d) for h in perm])
+    wqkv2 = np.concatenate([wqkv[:, part * E:(part + 1) * E][:, cols] for part in range(3)], axis=1)
+    wo2 = wo[cols]
+    o1, l1 = oracle.mha_block(x, wqkv, wo, H, True)
+    o2, l2 = oracle.mha_block(x, wqkv2, wo2, H, True)
+    np.testing.assert_allclose(o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l1[:, perm], l2, atol=1e-12)
