@@ -352,6 +352,98 @@ def run_decode(args, w: I.DecodeWorkload, ws: int, rank: int, local: int) -> int
     return 0
 
 
+def run_mha(args, w: I.MhaWorkload, ws: int, rank: int, local: int) -> int:
+    """The whole block: TFLOPS over projections + nominal attention flops."""
+    import torch
+    import torch.distributed as dist
+
+    import scaled_dot_product_18_b300 as sdp
+    sdp.load_library()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    x = I.make_mha_inputs(w)
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(torch.bfloat16)  # noqa: E731
+    tx, tw, to = dev(x.x), dev(x.w_qkv), dev(x.w_o)
+    kl = torch.from_numpy(x.key_lens).cuda() if x.key_lens is not None else None
+    out = torch.empty((w.B, w.N, w.E), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device="cuda")
+    nbytes = sdp.attn_mha_workspace_size(w.B, w.N, w.E)
+    wsbuf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def step():
+        st = sdp.attn_mha_fwd(tx, tw, to, out, lse, w.B, w.N, w.E, w.H, w.causal, kl, wsbuf, nbytes, sh)
+        if st != sdp.ATTN_OK:
+            raise sdp.AttnError(st, "attn_mha_fwd")
+
+    for _ in range(args.warmup):
+        step()
+    if sdp.attn_check_device(sh) != sdp.ATTN_OK:
+        raise RuntimeError("device error in warm-up")
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:  # noqa: BLE001
+        uuid = None
+    sampler = ClockSampler(uuid)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with sampler:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms_step = max_over_ranks(e0.elapsed_time(e1), ws, "cuda") / args.steps
+    if sdp.attn_check_device(sh) != sdp.ATTN_OK:
+        raise RuntimeError("device error in timed steps")
+    # end to end: x goes up, the block's output comes back (weights stay resident)
+    hx = torch.from_numpy(x.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        tx.copy_(hx, non_blocking=True)
+        step()
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(e2.elapsed_time(e3) / args.e2e_steps, ws, "cuda")
+    peaks = measured_peaks()
+    achieved = w.flops() / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": "mha_block_tflops", "value": job_tflops(w.flops(), ws, ms_step), "unit": "TFLOPS", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random weights)",
+        "config": {"workload": w.name, "B": w.B, "N": w.N, "E": w.E, "H": w.H, "causal": w.causal,
+                   "flops_per_step": w.flops()},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                     "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
+                     "kernel": "cuBLASLt projections + attn_fwd_kernel"},
+        "e2e": {"value": job_tflops(w.flops(), ws, ms_e2e), "unit": "TFLOPS", "h2d_bytes_per_step": hx.numel() * 2,
+                "d2h_bytes_per_step": hout.numel() * 2, "ms_per_step": ms_e2e},
+        "gpu_launches": args.steps,
+        "clocks": sampler.summary(),
+        "kernel_src_sha": kernel_source_sha(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -367,6 +459,8 @@ def main() -> int:
     ap.add_argument("--heads", type=int, default=None, help="override H (smaller cases for profiling)")
     ap.add_argument("--decode", default=None, choices=list(I.DECODE_WORKLOADS),
                     help="time attn_decode (one query per head against a K/V cache) instead")
+    ap.add_argument("--mha", default=None, choices=list(I.MHA_WORKLOADS),
+                    help="time attn_mha_fwd (QKV projection, attention, output projection) instead")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window (attn_fwd_window): query i sees keys j > i - window")
     args = ap.parse_args()
@@ -387,6 +481,8 @@ def main() -> int:
         return run_reference(args, w, ws, rank)
     if args.decode:
         return run_decode(args, I.DECODE_WORKLOADS[args.decode], ws, rank, local)
+    if args.mha:
+        return run_mha(args, I.MHA_WORKLOADS[args.mha], ws, rank, local)
 
     import torch
     import torch.distributed as dist

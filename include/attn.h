@@ -16,7 +16,8 @@
  *      softmax, the n x n score matrix is never written out).
  *
  * attn_fwd_window adds a sliding window (keys j > i - w only); attn_decode
- * computes one query per (batch, head) against a key/value cache.
+ * computes one query per (batch, head) against a key/value cache;
+ * attn_mha_fwd runs a whole multi-head self-attention block.
  *
  * Mask (attn_fwd): key j is visible to query i iff j < key_lens[b] (a key-padding mask,
  * lshu.cn "Self-attention meets the compute wall", sec. 4.1 and 5.2) and,
@@ -166,6 +167,42 @@ attn_status attn_decode_noalloc(const void *q, const void *k_cache, const void *
                                 void *out, float *lse,
                                 int B, int H, int L, int d, float scale,
                                 const int32_t *cache_lens, attn_stream_t stream);
+
+/*
+ * attn_mha_fwd -- a multi-head self-attention block without biases:
+ *
+ *   [Q | K | V] = x W_qkv,  heads split from the columns (head h = columns
+ *   h*d .. h*d+d-1 of each part),  O_h = attention(Q_h, K_h, V_h) with scale
+ *   1/sqrt(d) (the causal and key-length rules of attn_fwd),  merged heads
+ *   M = [O_0 | ... | O_{H-1}],  out = M W_o
+ *
+ * -- cnnetsun.cn "Transformer QKV bottlenecks on long sequences", sec. 2
+ *    (MinimalSelfAttention: Q/K/V projections, split heads, scaled dot-product
+ *    attention, merge, output projection); qqiyuan.cn "Multi-head attention in
+ *    the Transformer: implementation and performance optimisation" (one fused
+ *    [E, 3E] projection in place of three).
+ *
+ * x      : device bf16 [B, N, E] (E = H * d, d = 64 or 128, else
+ *          ATTN_EUNSUPPORTED; E % H != 0 -> ATTN_EINVAL).
+ * w_qkv  : device bf16 [E, 3E] row-major, Q, K, V column blocks in order.
+ * w_o    : device bf16 [E, E] row-major.
+ * out    : device bf16 [B, N, E].  lse: device fp32 [B, H, N] or NULL.
+ * key_lens: as in attn_fwd.  causal: as in attn_fwd.
+ * workspace: caller-owned device memory of attn_mha_workspace_size(B, N, E)
+ *          bytes (16-byte aligned) that the call overwrites: the bf16 Q/K/V
+ *          rows, the merged heads and the GEMM library's scratch.
+ * Q/K/V and M are bf16 tensors (fp32 accumulation, rounded to nearest even).
+ * The projections run in cuBLASLt, the attention in this library's kernel,
+ * which reads the heads straight out of the [B, N, 3E] rows through strided
+ * tensor maps (no transpose kernels).  Asynchronous on `stream`; the only
+ * allocation is cuBLASLt's host-side handle, created on the first call.
+ */
+attn_status attn_mha_fwd(const void *x, const void *w_qkv, const void *w_o, void *out, float *lse,
+                         int B, int N, int E, int H, int causal, const int32_t *key_lens,
+                         void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/* Bytes of workspace attn_mha_fwd needs (0 for invalid sizes). */
+size_t attn_mha_workspace_size(int B, int N, int E);
 
 /*
  * attn_check_device -- synchronise `stream`, then read and clear the

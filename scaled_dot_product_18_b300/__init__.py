@@ -28,7 +28,7 @@ ATTN_ETOOLARGE = -6
 
 # Symbols declared in include/attn.h.
 EXPORTS = ("attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_workspace_size", "attn_decode_noalloc",
-           "attn_check_device", "attn_status_str", "attn_abi_version")
+           "attn_mha_fwd", "attn_mha_workspace_size", "attn_check_device", "attn_status_str", "attn_abi_version")
 
 _lib = None
 
@@ -58,6 +58,10 @@ def load_library():
     lib.attn_decode_workspace_size.restype = ctypes.c_size_t
     lib.attn_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, vp, vp]
     lib.attn_decode_noalloc.restype = i
+    lib.attn_mha_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp, vp, ctypes.c_size_t, vp]
+    lib.attn_mha_fwd.restype = i
+    lib.attn_mha_workspace_size.argtypes = [i, i, i]
+    lib.attn_mha_workspace_size.restype = ctypes.c_size_t
     lib.attn_check_device.argtypes = [vp]
     lib.attn_check_device.restype = i
     lib.attn_status_str.argtypes = [i]
@@ -144,6 +148,19 @@ def decode(q, k_cache, v_cache, cache_lens=None, scale: float | None = None, str
     if st != ATTN_OK:
         raise AttnError(st, "attn_decode")
     return out, lse
+
+
+def attn_mha_fwd(x, w_qkv, w_o, out, lse, B: int, N: int, E: int, H: int, causal, key_lens=None,
+                 workspace=None, workspace_bytes: int = 0, stream=None) -> int:
+    """The C ``attn_mha_fwd``: projections, heads, attention, output projection."""
+    lib = load_library()
+    return lib.attn_mha_fwd(_ptr(x), _ptr(w_qkv), _ptr(w_o), _ptr(out), _ptr(lse), int(B), int(N), int(E), int(H),
+                            1 if causal else 0, _ptr(key_lens), _ptr(workspace), int(workspace_bytes),
+                            _stream(stream))
+
+
+def attn_mha_workspace_size(B: int, N: int, E: int) -> int:
+    return int(load_library().attn_mha_workspace_size(int(B), int(N), int(E)))
 
 
 def attn_check_device(stream=None) -> int:

@@ -33,8 +33,9 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if not force and not needs_build():
         return LIB
     tmp = LIB + ".tmp.%d" % os.getpid()
+    cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc())), "lib64")
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-I" + INCLUDE, "-o", tmp, *SOURCES]
+           "-I" + INCLUDE, "-o", tmp, *SOURCES, "-lcublasLt", "-Xlinker", "-rpath=" + cuda_lib]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.check_call(cmd)

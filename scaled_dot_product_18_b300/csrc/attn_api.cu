@@ -1,7 +1,9 @@
 // C ABI of the attention forward: argument checks on the host, tensor-map
 // encoding, launch, and the device error word.  The operation and every
 // argument are specified in include/attn.h.
+#include <cublasLt.h>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -114,9 +116,109 @@ attn_status forward(const void *q, const void *k, const void *v, void *out, floa
                           bhnd(H, N, d), stream);
 }
 
+// ------------------------------------------------------------- multi-head block
+
+cublasLtHandle_t lt_handle()
+{
+    static std::once_flag once;
+    static cublasLtHandle_t h = nullptr;
+    std::call_once(once, [] {
+        if (cublasLtCreate(&h) != CUBLAS_STATUS_SUCCESS) h = nullptr;
+    });
+    return h;
+}
+
+// Column-major D[m x n] = A[m x k] * B[k x n] (leading dimensions m, k, m),
+// bf16 in and out, fp32 accumulation, on cuBLASLt with the given workspace.
+// A row-major product C = X * W is the column-major W^T X^T, so callers pass
+// the row-major operands as (A, B) = (W, X).
+bool gemm_bf16(int m, int n, int k, const void *A, const void *Bm, void *D, void *ws, size_t ws_bytes,
+               cudaStream_t stream)
+{
+    cublasLtHandle_t h = lt_handle();
+    if (!h) return false;
+    cublasLtMatmulDesc_t op = nullptr;
+    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, ld = nullptr;
+    cublasLtMatmulPreference_t pref = nullptr;
+    bool ok = cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) == CUBLAS_STATUS_SUCCESS &&
+              cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, m, k, m) == CUBLAS_STATUS_SUCCESS &&
+              cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, k, n, k) == CUBLAS_STATUS_SUCCESS &&
+              cublasLtMatrixLayoutCreate(&ld, CUDA_R_16BF, m, n, m) == CUBLAS_STATUS_SUCCESS &&
+              cublasLtMatmulPreferenceCreate(&pref) == CUBLAS_STATUS_SUCCESS &&
+              cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws_bytes,
+                                                   sizeof(ws_bytes)) == CUBLAS_STATUS_SUCCESS;
+    cublasLtMatmulHeuristicResult_t res{};
+    int n_res = 0;
+    if (ok)
+        ok = cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, ld, ld, pref, 1, &res, &n_res) == CUBLAS_STATUS_SUCCESS &&
+             n_res > 0;
+    if (ok) {
+        const float alpha = 1.f, beta = 0.f;
+        ok = cublasLtMatmul(h, op, &alpha, A, la, Bm, lb, &beta, D, ld, D, ld, &res.algo, ws, ws_bytes, stream) ==
+             CUBLAS_STATUS_SUCCESS;
+    }
+    if (pref) cublasLtMatmulPreferenceDestroy(pref);
+    if (ld) cublasLtMatrixLayoutDestroy(ld);
+    if (lb) cublasLtMatrixLayoutDestroy(lb);
+    if (la) cublasLtMatrixLayoutDestroy(la);
+    if (op) cublasLtMatmulDescDestroy(op);
+    return ok;
+}
+
+constexpr size_t kGemmWorkspace = size_t(32) << 20;
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
 }  // namespace
 
 extern "C" {
+
+size_t attn_mha_workspace_size(int B, int N, int E)
+{
+    if (B <= 0 || N <= 0 || E <= 0) return 0;
+    const size_t rows = static_cast<size_t>(B) * N;
+    return round256(rows * 3 * E * 2) + round256(rows * E * 2) + kGemmWorkspace;
+}
+
+attn_status attn_mha_fwd(const void *x, const void *w_qkv, const void *w_o, void *out, float *lse, int B, int N,
+                         int E, int H, int causal, const int32_t *key_lens, void *workspace, size_t workspace_bytes,
+                         attn_stream_t stream)
+{
+    if (B < 0 || N < 0 || E <= 0 || H <= 0 || E % H != 0) return ATTN_EINVAL;
+    const int d = E / H;
+    if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
+    if (B == 0 || N == 0) return ATTN_OK;
+    if (!x || !w_qkv || !w_o || !out || !workspace) return ATTN_EINVAL;
+    const int64_t rows = static_cast<int64_t>(B) * N;
+    if (rows * 3 * E > INT32_MAX || static_cast<int64_t>(B) * H * ((N + 127) / 128) > INT32_MAX) return ATTN_EINVAL;
+    if (workspace_bytes < attn_mha_workspace_size(B, N, E)) return ATTN_EINVAL;
+    if (misaligned(x) || misaligned(w_qkv) || misaligned(w_o) || misaligned(out) || misaligned(workspace))
+        return ATTN_EALIGN;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return ATTN_EALIGN;
+    if (key_lens && (reinterpret_cast<uintptr_t>(key_lens) & 3u)) return ATTN_EALIGN;
+
+    char *ws = static_cast<char *>(workspace);
+    const size_t qkv_bytes = round256(static_cast<size_t>(rows) * 3 * E * 2);
+    auto *qkv = reinterpret_cast<__nv_bfloat16 *>(ws);
+    auto *attn = reinterpret_cast<__nv_bfloat16 *>(ws + qkv_bytes);
+    void *gemm_ws = ws + qkv_bytes + round256(static_cast<size_t>(rows) * E * 2);
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    // 1. [Q | K | V] = x W_qkv: rows of [B*N, 3E], head h at columns h*d of each part.
+    if (!gemm_bf16(3 * E, static_cast<int>(rows), E, w_qkv, x, qkv, gemm_ws, kGemmWorkspace, s)) return ATTN_ECUDA;
+    // 2. Attention straight from the interleaved rows ([B, N, H, d] views), the
+    //    merged heads written as rows of [B*N, E].
+    const Strides in_st{3 * static_cast<int64_t>(E), d, static_cast<int64_t>(N) * 3 * E};
+    const Strides out_st{E, d, static_cast<int64_t>(N) * E};
+    const attn_status st = launch_forward(qkv, qkv + E, qkv + 2 * E, attn, lse, B, H, N, d,
+                                          static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))), causal,
+                                          key_lens, 0, in_st, out_st, stream);
+    if (st != ATTN_OK) return st;
+    // 3. out = merged W_o.
+    if (!gemm_bf16(E, static_cast<int>(rows), E, w_o, attn, out, gemm_ws, kGemmWorkspace, s)) return ATTN_ECUDA;
+    return ATTN_OK;
+}
+
 
 attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse, int B, int H, int N, int d,
                      float scale, int causal, const int32_t *key_lens, attn_stream_t stream)

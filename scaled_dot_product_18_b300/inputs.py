@@ -260,3 +260,54 @@ def make_decode_inputs(w: DecodeWorkload, seed: int | None = None) -> HostInputs
     v = make_tensor_bits(s, STREAM_V, (w.B, w.H, w.L, w.d))
     cl = make_key_lens(s, w.B, *w.cache_len_range) if w.cache_len_range else None
     return HostInputs(q, k, v, cl)
+
+
+@dataclasses.dataclass(frozen=True)
+class MhaWorkload:
+    """A multi-head self-attention block: x [B, N, E] ~ N(0, 1), projection
+    weights ~ N(0, 1/E) (so Q, K, V and the output stay O(1)), H heads of
+    d = E/H, causal flag and optional per-batch key lengths."""
+    name: str
+    B: int
+    N: int
+    E: int
+    H: int
+    causal: bool
+    key_len_range: tuple[int, int] | None = None
+    seed: int = 0
+
+    @property
+    def d(self) -> int:
+        return self.E // self.H
+
+    def flops(self) -> float:
+        """Projections 2*B*N*E*4E plus nominal attention 4*B*H*N^2*d (halved for causal)."""
+        att = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return 2.0 * self.B * self.N * self.E * 4 * self.E + (att / 2 if self.causal else att)
+
+
+MHA_WORKLOADS = {
+    # cnnetsun.cn's MinimalSelfAttention check: input (2, 100, 512), 8 heads
+    "mha_b2n100e512h8": MhaWorkload("mha_b2n100e512h8", 2, 100, 512, 8, False),
+    # BERT-base-like block (embed 768, 12 heads) with padded sequences
+    "mha_b16n512e768h12_keylens": MhaWorkload("mha_b16n512e768h12_keylens", 16, 512, 768, 12, False, (256, 512)),
+    # long-context block with 32 heads of 128 (embed 4096), causal
+    "mha_b1n16384e4096h32_causal": MhaWorkload("mha_b1n16384e4096h32_causal", 1, 16384, 4096, 32, True),
+}
+
+
+@dataclasses.dataclass
+class MhaInputs:
+    x: np.ndarray       # bf16 bits [B, N, E]
+    w_qkv: np.ndarray   # bf16 bits [E, 3E]
+    w_o: np.ndarray     # bf16 bits [E, E]
+    key_lens: np.ndarray | None
+
+
+def make_mha_inputs(w: MhaWorkload, seed: int | None = None) -> MhaInputs:
+    s = w.seed if seed is None else seed
+    x = make_tensor_bits(s, STREAM_Q, (w.B, w.N, w.E))
+    wqkv = make_tensor_bits(s, STREAM_K, (w.E, 3 * w.E), amplitude=1.0 / float(np.sqrt(w.E)))
+    wo = make_tensor_bits(s, STREAM_V, (w.E, w.E), amplitude=1.0 / float(np.sqrt(w.E)))
+    kl = make_key_lens(s, w.B, *w.key_len_range) if w.key_len_range else None
+    return MhaInputs(x, wqkv, wo, kl)

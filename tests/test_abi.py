@@ -29,8 +29,8 @@ def declared_functions():
 
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert {"attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_workspace_size", "attn_check_device",
-            "attn_status_str", "attn_abi_version"} <= names
+    assert {"attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_workspace_size", "attn_mha_fwd",
+            "attn_mha_workspace_size", "attn_check_device", "attn_status_str", "attn_abi_version"} <= names
     assert names == set(sdp.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
@@ -125,6 +125,33 @@ def test_decode_host_side_rejections(lib, args, want):
     st = lib.attn_decode(a["q"], a["k"], a["v"], a["out"], a["lse"], a["B"], a["H"], a["L"], a["d"], a["scale"],
                          a["cl"], a["ws"], a["ws_bytes"], a["stream"])
     assert st == want, (args, st)
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(E=96, H=1), sdp.ATTN_EUNSUPPORTED),   # d = 96
+    (dict(E=512, H=3), sdp.ATTN_EINVAL),        # E % H != 0
+    (dict(H=0), sdp.ATTN_EINVAL),
+    (dict(B=-1), sdp.ATTN_EINVAL),
+    (dict(x=None), sdp.ATTN_EINVAL),
+    (dict(wo=None), sdp.ATTN_EINVAL),
+    (dict(ws=None), sdp.ATTN_EINVAL),
+    (dict(ws_bytes=1024), sdp.ATTN_EINVAL),
+    (dict(x=P + 2), sdp.ATTN_EALIGN),
+    (dict(out=P + 8), sdp.ATTN_EALIGN),
+    (dict(B=0, x=None, ws=None), sdp.ATTN_OK),
+])
+def test_mha_host_side_rejections(lib, args, want):
+    a = dict(x=P, wqkv=P, wo=P, out=P, lse=None, B=2, N=100, E=512, H=8, causal=0, kl=None, ws=P,
+             ws_bytes=1 << 40, stream=None)
+    a.update(args)
+    st = lib.attn_mha_fwd(a["x"], a["wqkv"], a["wo"], a["out"], a["lse"], a["B"], a["N"], a["E"], a["H"],
+                          a["causal"], a["kl"], a["ws"], a["ws_bytes"], a["stream"])
+    assert st == want, (args, st)
+
+
+def test_mha_workspace_size(lib):
+    n = sdp.attn_mha_workspace_size(2, 100, 512)
+    assert n >= 2 * 100 * 512 * 2 * 4 and sdp.attn_mha_workspace_size(0, 100, 512) == 0
 
 
 def test_binding_raises_without_library(tmp_path, monkeypatch):

@@ -1,0 +1,68 @@
+"""GPU parity of attn_mha_fwd (fused QKV projection, heads, attention, output
+projection) with the fp64 block oracle, which rounds Q/K/V and the merged
+heads to bf16 at the same two points."""
+import numpy as np
+import pytest
+
+import oracle
+import scaled_dot_product_18_b300 as sdp
+from scaled_dot_product_18_b300 import inputs as I
+
+from gpu_util import MAX_ABS, REL_L2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+# Q/K/V are bf16 roundings of fp32 GEMM sums on the GPU and of exact sums in
+# the oracle; where an exact sum lies within the fp32 error of a bf16
+# rounding midpoint the two round one ulp (2^-8 relative) apart.  One such q
+# or k element moves a logit by at most 2^-8 |q_t k_t| / sqrt(d); with
+# |q_t|, |k_t| <= 5 and d >= 64 that is 0.012, which bounds the shift of a
+# row's log-sum-exp.  The block's output is held to the attention tolerances.
+BLOCK_LSE_ABS = 1.2e-2
+
+
+def run_mha(w: I.MhaWorkload, x: I.MhaInputs):
+    import torch
+    tx, tw, to = to_dev(x.x), to_dev(x.w_qkv), to_dev(x.w_o)
+    out = torch.full((w.B, w.N, w.E), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((w.B, w.H, w.N), float("nan"), dtype=torch.float32, device="cuda")
+    nbytes = sdp.attn_mha_workspace_size(w.B, w.N, w.E)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    kl = torch.from_numpy(x.key_lens).cuda() if x.key_lens is not None else None
+    st = sdp.attn_mha_fwd(tx, tw, to, out, lse, w.B, w.N, w.E, w.H, w.causal, kl, ws, nbytes,
+                          torch.cuda.current_stream())
+    assert st == sdp.ATTN_OK, sdp.attn_status_str(st)
+    assert sdp.attn_check_device(torch.cuda.current_stream()) == sdp.ATTN_OK
+    return out.float().cpu().numpy().astype(np.float64), lse.cpu().numpy().astype(np.float64)
+
+
+def check(out, lse, out_ref, lse_ref, what):
+    assert not np.isnan(out).any() and not np.isnan(lse).any(), what
+    err = float(np.abs(out - out_ref).max())
+    rel = float(np.linalg.norm(out - out_ref) / np.linalg.norm(out_ref))
+    assert err <= MAX_ABS, "%s: max-abs %.3e" % (what, err)
+    assert rel <= REL_L2, "%s: rel-L2 %.3e" % (what, rel)
+    assert float(np.abs(lse - lse_ref).max()) <= BLOCK_LSE_ABS, what
+    assert float(np.median(np.abs(lse - lse_ref))) <= 1e-4, what  # flips are rare: most rows agree closely
+
+
+@pytest.mark.parametrize("name", ["mha_b2n100e512h8", "mha_b16n512e768h12_keylens"])
+def test_mha_workloads(name):
+    w = I.MHA_WORKLOADS[name]
+    x = I.make_mha_inputs(w)
+    out, lse = run_mha(w, x)
+    out_ref, lse_ref = oracle.mha_block(x.x, x.w_qkv, x.w_o, w.H, w.causal, x.key_lens)
+    check(out, lse, out_ref, lse_ref, name)
+
+
+@pytest.mark.parametrize("B,N,E,H,causal,lens", [
+    (1, 300, 1024, 8, True, None),
+    (3, 257, 256, 2, False, (1, 257)),
+    (2, 129, 384, 6, True, (100, 129)),
+])
+def test_mha_shapes(B, N, E, H, causal, lens):
+    w = I.MhaWorkload("t", B, N, E, H, causal, lens, seed=B * 7 + N)
+    x = I.make_mha_inputs(w)
+    out, lse = run_mha(w, x)
+    out_ref, lse_ref = oracle.mha_block(x.x, x.w_qkv, x.w_o, w.H, w.causal, x.key_lens)
+    check(out, lse, out_ref, lse_ref, "B=%d N=%d E=%d H=%d" % (B, N, E, H))
