@@ -194,3 +194,73 @@ def mha_block(x, w_qkv, w_o, H: int, causal: bool, key_lens=None, threads: int |
     O, lse = attention_rows(q, k, v, 1.0 / np.sqrt(d), causal, key_lens, threads=threads)
     attn = round_bf16(O.transpose(0, 2, 1, 3).reshape(B, N, E))  # merge heads
     return np.matmul(attn, w_o), lse
+
+
+def attention_backward_literal(q, k, v, dout, scale: float, causal: bool, key_lens=None):
+    """Gradients of the attention forward with respect to Q, K and V, float64,
+    from the materialised score matrix (tiny and moderate sizes):
+
+        P = softmax(S), S = scale Q K^T (hidden keys excluded)
+        dV = P^T dO,  dP = dO V^T,  D_i = sum_j P_ij dP_ij,
+        dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q
+
+    (the chain rule through O = P V and the softmax; the pages reuse the
+    softmax output in the backward pass, hotelren.com sec. 4.2).  Rows with
+    no visible key contribute nothing.  Returns (dQ, dK, dV).
+    """
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    _, _, P = attention_literal(q, k, v, scale, causal, key_lens)
+    dV = np.matmul(np.swapaxes(P, -1, -2), dout)
+    dP = np.matmul(dout, np.swapaxes(v, -1, -2))
+    D = (P * dP).sum(-1, keepdims=True)
+    dS = P * (dP - D)
+    dQ = scale * np.matmul(dS, k)
+    dK = scale * np.matmul(np.swapaxes(dS, -1, -2), q)
+    return dQ, dK, dV
+
+
+def attention_backward_sampled(q, k, v, dout, scale: float, causal: bool, key_lens=None, heads=None,
+                               q_rows=None, k_rows=None):
+    """The same gradients for selected (b, h) heads, dQ rows and dK/dV rows,
+    without the full N x N matrix: each row of P is rebuilt from the row
+    oracle's log-sum-exp, P_ij = exp(s_ij - lse_i) over the visible keys.
+    Returns dicts keyed by (b, h): dQ [len(q_rows), d], dK and dV
+    [len(k_rows), d]."""
+    q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    B, H, N, d = q.shape
+    out = {}
+    for b, h in heads:
+        kl = N if key_lens is None else int(key_lens[b])
+        O, lse = attention_rows(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], scale, causal,
+                                None if key_lens is None else np.array([kl], dtype=np.int32))
+        O, lse = O[0, 0], lse[0, 0]
+        Dvec = (dout[b, h] * O).sum(-1)  # D_i = sum_j P_ij dP_ij = dO_i . O_i
+        qb, kb, vb, db = q[b, h], k[b, h], v[b, h], dout[b, h]
+
+        def p_row(i):  # P[i, :] over all keys (zeros where hidden)
+            keep = np.arange(N) < kl
+            if causal:
+                keep &= np.arange(N) <= i
+            if not np.isfinite(lse[i]):
+                return np.zeros(N)
+            s = scale * (kb @ qb[i])
+            return np.where(keep, np.exp(np.where(keep, s, 0.0) - lse[i]), 0.0)
+
+        dQ = np.zeros((len(q_rows), d))
+        for r, i in enumerate(q_rows):
+            p = p_row(i)
+            dp = vb @ db[i]
+            dQ[r] = scale * ((p * (dp - Dvec[i])) @ kb)
+        dK = np.zeros((len(k_rows), d))
+        dV = np.zeros((len(k_rows), d))
+        for r, j in enumerate(k_rows):
+            col = np.zeros(N)  # P[:, j]
+            for i in range(N):
+                if j < kl and (not causal or j <= i) and np.isfinite(lse[i]):
+                    col[i] = np.exp(scale * (qb[i] @ kb[j]) - lse[i])
+            dpj = db @ vb[j]  # dP[:, j]
+            ds = col * (dpj - Dvec)
+            dV[r] = col @ db
+            dK[r] = scale * (ds @ qb)
+        out[(b, h)] = (dQ, dK, dV)
+    return out

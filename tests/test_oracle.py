@@ -455,3 +455,62 @@ def test_mha_block_head_permutation_invariance():
     o2, l2 = oracle.mha_block(x, wqkv2, wo2, H, True)
     np.testing.assert_allclose(o1, o2, atol=1e-12)
     np.testing.assert_allclose(l1[:, perm], l2, atol=1e-12)
+
+
+# --- backward: gradients of the forward ------------------------------------------
+
+def _loss(q, k, v, g, scale, causal, kl):
+    O, _, _ = oracle.attention_literal(q, k, v, scale, causal, kl)
+    return float((O * g).sum())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_finite_differences(causal):
+    # d(sum(O * G))/dX by central differences, element by element.
+    r = np.random.default_rng(61)
+    B, H, N, d = 1, 2, 5, 3
+    q, k, v, g = (r.standard_normal((B, H, N, d)) for _ in range(4))
+    kl = np.array([4], dtype=np.int32)
+    dQ, dK, dV = oracle.attention_backward_literal(q, k, v, g, 0.7, causal, kl)
+    eps = 1e-6
+    for X, dX in ((q, dQ), (k, dK), (v, dV)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            old = X[idx]
+            X[idx] = old + eps
+            up = _loss(q, k, v, g, 0.7, causal, kl)
+            X[idx] = old - eps
+            dn = _loss(q, k, v, g, 0.7, causal, kl)
+            X[idx] = old
+            num[idx] = (up - dn) / (2 * eps)
+        np.testing.assert_allclose(dX, num, atol=1e-7)
+    assert np.all(dK[:, :, 4:] == 0.0) and np.all(dV[:, :, 4:] == 0.0)  # hidden keys get no gradient
+
+
+def test_backward_sampled_matches_literal():
+    r = np.random.default_rng(62)
+    B, H, N, d = 2, 2, 37, 8
+    q, k, v, g = (r.standard_normal((B, H, N, d)) for _ in range(4))
+    kl = np.array([30, 37], dtype=np.int32)
+    for causal in (False, True):
+        dQ, dK, dV = oracle.attention_backward_literal(q, k, v, g, 0.4, causal, kl)
+        rows = [0, 5, 29, 36]
+        got = oracle.attention_backward_sampled(q, k, v, g, 0.4, causal, kl, heads=[(0, 1), (1, 0)], q_rows=rows,
+                                                k_rows=rows)
+        for (b, h), (sq, sk, sv) in got.items():
+            np.testing.assert_allclose(sq, dQ[b, h, rows], atol=1e-11)
+            np.testing.assert_allclose(sk, dK[b, h, rows], atol=1e-11)
+            np.testing.assert_allclose(sv, dV[b, h, rows], atol=1e-11)
+
+
+def test_backward_uniform_attention_closed_form():
+    # Q = 0: P is uniform over the visible keys, so dV_j = (1/n) sum over the
+    # rows that see key j of dO_i, computed here with explicit counts.
+    r = np.random.default_rng(63)
+    B, H, N, d = 1, 1, 6, 2
+    k, v, g = (r.standard_normal((B, H, N, d)) for _ in range(3))
+    q = np.zeros_like(k)
+    _, _, dV = oracle.attention_backward_literal(q, k, v, g, 1.0, True)
+    for j in range(N):
+        want = sum(g[0, 0, i] / (i + 1) for i in range(j, N))
+        np.testing.assert_allclose(dV[0, 0, j], want, atol=1e-12)
