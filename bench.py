@@ -444,6 +444,107 @@ def run_mha(args, w: I.MhaWorkload, ws: int, rank: int, local: int) -> int:
     return 0
 
 
+def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
+    """The backward (dQ, dK, dV) of one workload: TFLOPS over the nominal
+    backward flops, 2.5x the forward's (five N x N x d contractions per head
+    instead of two: S, dP, dV, dK, dQ), halved when causal."""
+    import torch
+    import torch.distributed as dist
+
+    import scaled_dot_product_18_b300 as sdp
+    sdp.load_library()
+    torch.cuda.set_device(local)
+    if ws > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    x = I.make_inputs(w)
+    hdo = I.make_dout(w)
+    dev = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(torch.bfloat16)  # noqa: E731
+    q, k, v, do = dev(x.q), dev(x.k), dev(x.v), dev(hdo)
+    kl = torch.from_numpy(x.key_lens).cuda() if x.key_lens is not None else None
+    out, lse = sdp.attention(q, k, v, causal=w.causal, key_lens=kl, scale=w.scale)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    nbytes = sdp.attn_bwd_workspace_size(w.B, w.H, w.N, w.d)
+    wsbuf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+
+    def step():
+        st = sdp.attn_bwd(q, k, v, out, do, lse, dq, dk, dv, w.B, w.H, w.N, w.d, w.scale, w.causal, kl, wsbuf,
+                          nbytes, sh)
+        if st != sdp.ATTN_OK:
+            raise sdp.AttnError(st, "attn_bwd")
+
+    for _ in range(args.warmup):
+        step()
+    if sdp.attn_check_device(sh) != sdp.ATTN_OK:
+        raise RuntimeError("device error in warm-up")
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:  # noqa: BLE001
+        uuid = None
+    sampler = ClockSampler(uuid)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with sampler:
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms_step = max_over_ranks(e0.elapsed_time(e1), ws, "cuda") / args.steps
+    if sdp.attn_check_device(sh) != sdp.ATTN_OK:
+        raise RuntimeError("device error in timed steps")
+    # end to end: q, k, v, O, dO and lse go up, dQ, dK, dV come back
+    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
+    hin = [pin(t) for t in (q, k, v, out, do, lse)]
+    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+
+    def e2e_step():
+        for d_, h_ in zip((q, k, v, out, do, lse), hin):
+            d_.copy_(h_, non_blocking=True)
+        step()
+        for h_, d_ in zip(hout, (dq, dk, dv)):
+            h_.copy_(d_, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e3.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(e2.elapsed_time(e3) / args.e2e_steps, ws, "cuda")
+    peaks = measured_peaks()
+    flops = 2.5 * w.flops()
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    line = {
+        "metric": "attention_bwd_tflops", "value": job_tflops(flops, ws, ms_step), "unit": "TFLOPS", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name + "_backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+                   "flops_per_step": flops, "l2": "inputs larger than L2"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                     "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
+                     "kernel": "attn_bwd_kernel (+ bwd_prepare, bwd_finish)"},
+        "e2e": {"value": job_tflops(flops, ws, ms_e2e), "unit": "TFLOPS",
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in hin),
+                "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in hout), "ms_per_step": ms_e2e},
+        "gpu_launches": 3 * args.steps,
+        "clocks": sampler.summary(),
+        "kernel_src_sha": kernel_source_sha(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
 def main() -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -463,6 +564,8 @@ def main() -> int:
                     help="time attn_mha_fwd (QKV projection, attention, output projection) instead")
     ap.add_argument("--window", type=int, default=0,
                     help="sliding window (attn_fwd_window): query i sees keys j > i - window")
+    ap.add_argument("--backward", action="store_true",
+                    help="time attn_bwd (dQ, dK, dV of --config) instead of the forward")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -483,6 +586,8 @@ def main() -> int:
         return run_decode(args, I.DECODE_WORKLOADS[args.decode], ws, rank, local)
     if args.mha:
         return run_mha(args, I.MHA_WORKLOADS[args.mha], ws, rank, local)
+    if args.backward:
+        return run_backward(args, w, ws, rank, local)
 
     import torch
     import torch.distributed as dist

@@ -205,6 +205,44 @@ attn_status attn_mha_fwd(const void *x, const void *w_qkv, const void *w_o, void
 size_t attn_mha_workspace_size(int B, int N, int E);
 
 /*
+ * attn_bwd -- gradients of attn_fwd with respect to q, k and v:
+ *
+ *   P = softmax(scale q k^T + mask) (rebuilt from lse, never stored),
+ *   dV = P^T dO,  dP = dO V^T,  D_i = dO_i . O_i,  dS = P * (dP - D),
+ *   dQ = scale dS K,  dK = scale dS^T Q
+ *
+ * -- the chain rule through O = P V and the row softmax; the backward pass
+ *    reuses the softmax probabilities kept from the forward (hotelren.com
+ *    "AI attention: essence and evolution", sec. 4.2), here recomputed from
+ *    the forward's log-sum-exp so that no N x N matrix exists.
+ *
+ * q, k, v : device bf16 [B, H, N, d] contiguous, the forward's inputs.
+ * out     : device bf16 [B, H, N, d], the forward's output for q, k, v.
+ * dout    : device bf16 [B, H, N, d], the gradient of the loss w.r.t. out.
+ * lse     : device fp32 [B, H, N], the forward's log-sum-exp (not NULL).
+ * dq, dk, dv: device bf16 [B, H, N, d], written (fp32 accumulation, rounded
+ *           to nearest even).  Rows of dk/dv for hidden keys are 0; rows of
+ *           dq for queries with no visible key are 0.
+ * B, H, N, d, scale, causal, key_lens: as in attn_fwd (same checks, same
+ *           errors).
+ * workspace: caller-owned device memory of attn_bwd_workspace_size(B, H, N, d)
+ *           bytes, 16-byte aligned, overwritten by the call (an fp32 dQ
+ *           accumulator and the D vector).
+ * Three launches on `stream` (D and accumulator reset; one CTA per 128 keys
+ * of one head accumulating dK, dV in tensor memory and adding dQ partials
+ * with fp32 atomics; dQ conversion).  The order of the fp32 dQ additions is
+ * not fixed, so dq may differ between runs in the last bf16 place.
+ */
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                     const float *lse, void *dq, void *dk, void *dv,
+                     int B, int H, int N, int d, float scale, int causal,
+                     const int32_t *key_lens, void *workspace, size_t workspace_bytes,
+                     attn_stream_t stream);
+
+/* Bytes of workspace attn_bwd needs (0 for invalid sizes). */
+size_t attn_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
  * attn_check_device -- synchronise `stream`, then read and clear the
  * library's device error word on the current device.  Returns ATTN_EDEVICE
  * if a kernel since the last check gave up on a bounded wait (its outputs are
@@ -218,7 +256,7 @@ const char *attn_status_str(attn_status s);
 /* ABI version of this header (bumped on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 3
+#define ATTN_ABI_VERSION 4
 
 #ifdef __cplusplus
 }

@@ -196,7 +196,7 @@ def mha_block(x, w_qkv, w_o, H: int, causal: bool, key_lens=None, threads: int |
     return np.matmul(attn, w_o), lse
 
 
-def attention_backward_literal(q, k, v, dout, scale: float, causal: bool, key_lens=None):
+def attention_backward_literal(q, k, v, dout, scale: float, causal: bool, key_lens=None, out=None):
     """Gradients of the attention forward with respect to Q, K and V, float64,
     from the materialised score matrix (tiny and moderate sizes):
 
@@ -207,12 +207,20 @@ def attention_backward_literal(q, k, v, dout, scale: float, causal: bool, key_le
     (the chain rule through O = P V and the softmax; the pages reuse the
     softmax output in the backward pass, hotelren.com sec. 4.2).  Rows with
     no visible key contribute nothing.  Returns (dQ, dK, dV).
+
+    out: optional stored forward output [B, H, N, d] (for instance bf16 bit
+    patterns).  When given, D_i is taken as dO_i . out_i -- the identity
+    sum_j P_ij dP_ij = dO_i . (P V)_i applied to that stored output -- instead
+    of from P and dP; everything else is unchanged.
     """
     q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
     _, _, P = attention_literal(q, k, v, scale, causal, key_lens)
     dV = np.matmul(np.swapaxes(P, -1, -2), dout)
     dP = np.matmul(dout, np.swapaxes(v, -1, -2))
-    D = (P * dP).sum(-1, keepdims=True)
+    if out is None:
+        D = (P * dP).sum(-1, keepdims=True)
+    else:
+        D = (dout * _as_f64(out)).sum(-1, keepdims=True)
     dS = P * (dP - D)
     dQ = scale * np.matmul(dS, k)
     dK = scale * np.matmul(np.swapaxes(dS, -1, -2), q)
@@ -220,20 +228,24 @@ def attention_backward_literal(q, k, v, dout, scale: float, causal: bool, key_le
 
 
 def attention_backward_sampled(q, k, v, dout, scale: float, causal: bool, key_lens=None, heads=None,
-                               q_rows=None, k_rows=None):
+                               q_rows=None, k_rows=None, out=None):
     """The same gradients for selected (b, h) heads, dQ rows and dK/dV rows,
     without the full N x N matrix: each row of P is rebuilt from the row
     oracle's log-sum-exp, P_ij = exp(s_ij - lse_i) over the visible keys.
-    Returns dicts keyed by (b, h): dQ [len(q_rows), d], dK and dV
-    [len(k_rows), d]."""
+    out: optional stored forward output [B, H, N, d]; D_i is then dO_i . out_i
+    (as in attention_backward_literal).  Returns dicts keyed by (b, h): dQ
+    [len(q_rows), d], dK and dV [len(k_rows), d]."""
     q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
+    stored = out
     B, H, N, d = q.shape
-    out = {}
+    res = {}
     for b, h in heads:
         kl = N if key_lens is None else int(key_lens[b])
         O, lse = attention_rows(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], scale, causal,
                                 None if key_lens is None else np.array([kl], dtype=np.int32))
         O, lse = O[0, 0], lse[0, 0]
+        if stored is not None:
+            O = _as_f64(stored[b, h])
         Dvec = (dout[b, h] * O).sum(-1)  # D_i = sum_j P_ij dP_ij = dO_i . O_i
         qb, kb, vb, db = q[b, h], k[b, h], v[b, h], dout[b, h]
 
@@ -262,5 +274,5 @@ def attention_backward_sampled(q, k, v, dout, scale: float, causal: bool, key_le
             ds = col * (dpj - Dvec)
             dV[r] = col @ db
             dK[r] = scale * (ds @ qb)
-        out[(b, h)] = (dQ, dK, dV)
-    return out
+        res[(b, h)] = (dQ, dK, dV)
+    return res

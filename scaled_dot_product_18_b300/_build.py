@@ -10,7 +10,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libattn.so")
-SOURCES = [os.path.join(CSRC, f) for f in ("attn_fwd_sm103.cu", "attn_decode_sm103.cu", "attn_api.cu")]
+SOURCES = [os.path.join(CSRC, f) for f in ("attn_fwd_sm103.cu", "attn_bwd_sm103.cu", "attn_decode_sm103.cu",
+                                           "attn_api.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("ptx_sm103.cuh", "attn_internal.h")] + [os.path.join(INCLUDE, "attn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -286,12 +286,71 @@ attn_status attn_decode(const void *q, const void *k_cache, const void *v_cache,
     return rc == 0 ? ATTN_OK : ATTN_ECUDA;
 }
 
+size_t attn_bwd_workspace_size(int B, int H, int N, int d)
+{
+    if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    return round256(rows * d * sizeof(float)) + round256(rows * sizeof(float));
+}
+
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
+                     void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal,
+                     const int32_t *key_lens, void *workspace, size_t workspace_bytes, attn_stream_t stream)
+{
+    if (B < 0 || H < 0 || N < 0) return ATTN_EINVAL;
+    if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_EINVAL;
+    if (B == 0 || H == 0 || N == 0) return ATTN_OK;
+    if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv || !workspace) return ATTN_EINVAL;
+    const int64_t bh = static_cast<int64_t>(B) * H;
+    const int64_t tiles = (static_cast<int64_t>(N) + 127) / 128;
+    if (bh > INT32_MAX || tiles * bh > INT32_MAX || bh * N * d > (int64_t(1) << 40)) return ATTN_EINVAL;
+    if (workspace_bytes < attn_bwd_workspace_size(B, H, N, d)) return ATTN_EINVAL;
+    for (const void *p : {q, k, v, out, dout, static_cast<const void *>(dq), static_cast<const void *>(dk),
+                          static_cast<const void *>(dv), static_cast<const void *>(workspace)})
+        if (misaligned(p)) return ATTN_EALIGN;
+    if (reinterpret_cast<uintptr_t>(lse) & 3u) return ATTN_EALIGN;
+    if (key_lens && (reinterpret_cast<uintptr_t>(key_lens) & 3u)) return ATTN_EALIGN;
+
+    const Strides st = bhnd(H, N, d);
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_map(&tq, q, B, H, N, d, st) || !make_map(&tk, k, B, H, N, d, st) || !make_map(&tv, v, B, H, N, d, st) ||
+        !make_map(&tdo, dout, B, H, N, d, st))
+        return ATTN_ECUDA;
+    const size_t rows = static_cast<size_t>(bh) * N;
+    sdp18::BwdLaunch a{};
+    a.tm_q = &tq;
+    a.tm_k = &tk;
+    a.tm_v = &tv;
+    a.tm_do = &tdo;
+    a.out = out;
+    a.dout = dout;
+    a.lse = lse;
+    a.dqacc = static_cast<float *>(workspace);
+    a.dvec = reinterpret_cast<float *>(static_cast<char *>(workspace) + round256(rows * d * sizeof(float)));
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.key_lens = key_lens;
+    a.B = B;
+    a.H = H;
+    a.N = N;
+    a.d = d;
+    a.scale = scale;
+    a.causal = causal ? 1 : 0;
+    a.stream = reinterpret_cast<cudaStream_t>(stream);
+    const int rc = sdp18::attn_bwd_launch(a);
+    if (rc == -2) return ATTN_EUNSUPPORTED;
+    return rc == 0 ? ATTN_OK : ATTN_ECUDA;
+}
+
 attn_status attn_check_device(attn_stream_t stream)
 {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ECUDA;
-    int v = 0;
+    int v = 0, vb = 0;
     if (sdp18::read_and_clear_device_error(&v) != 0) return ATTN_ECUDA;
-    return v != 0 ? ATTN_EDEVICE : ATTN_OK;
+    if (sdp18::read_and_clear_bwd_error(&vb) != 0) return ATTN_ECUDA;
+    return (v != 0 || vb != 0) ? ATTN_EDEVICE : ATTN_OK;
 }
 
 const char *attn_status_str(attn_status s)

@@ -1,0 +1,469 @@
+// Attention backward for B300 (sm_103a): dQ, dK, dV of the forward in
+// attn_fwd_sm103.cu, recomputing P from the saved log-sum-exp instead of
+// storing it (the pages reuse the forward's softmax statistics in the
+// backward pass, hotelren.com "AI attention: essence and evolution",
+// sec. 4.2).
+//
+// With S = scale Q K^T, P = softmax(S), O = P V and the loss gradient dO:
+//   dV = P^T dO,  dP = dO V^T,  D_i = sum_j P_ij dP_ij = dO_i . O_i,
+//   dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q.
+//
+// One CTA owns a 128-key tile of one (batch, head) and walks the query tiles
+// that can see it (all of them, or those at or after the diagonal when
+// causal).  Per query tile, in tensor memory (512 columns):
+//   S^T = K Q_i^T          columns   0..127  (keys in TMEM lanes)
+//   dP^T = V dO_i^T        columns 128..255
+//   P^T -> bf16 over the first 64 columns of S^T (A operand of dV += P^T dO_i)
+//   dS^T -> bf16 in shared memory (A operand of dK += dS^T Q_i, and, read
+//          query-major, of dQ_i = dS K, which lands in the dP^T columns)
+//   dV, dK accumulate in columns 256.. across the query tiles.
+// dQ_i is added (times scale) to an fp32 accumulator in global memory with
+// vector reductions; a pre-pass computes D and clears the accumulator, a
+// post-pass converts it to bf16.
+//
+//   warps 0-3  key row r = thread (TMEM lane r): P^T, dS^T, dQ reduction,
+//              the dK / dV epilogue.
+//   warp 4     TMA producer: K, V once; Q_i, dO_i through a 2-stage ring.
+//   warp 5     allocates TMEM and issues the five MMAs of each query tile.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "attn_internal.h"
+#include "ptx_sm103.cuh"
+
+namespace sdp18 {
+
+// Device error word of the backward kernel (each translation unit keeps its own
+// word: the library is built without relocatable device code).
+__device__ int g_sdp18_bwd_error = 0;
+
+namespace {
+
+constexpr int kKeys = 128;    // keys per CTA
+constexpr int kQTile = 128;   // queries per step
+constexpr int kThreads = 192;
+constexpr int kTmaWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTS = 0, kTDP = 128, kTDV = 256;  // dK at kTDV + D
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct BwdSmem {
+    static constexpr int kTileBytes = 128 * D * 2;  // one [128 x D] bf16 tile
+    static constexpr int kStages = 2;               // (Q_i, dO_i) stages
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kTileBytes;
+    static constexpr int kOffRing = kOffV + kTileBytes;  // stage s: Q at +0, dO at +kTileBytes
+    static constexpr int kOffDS = kOffRing + kStages * 2 * kTileBytes;  // [128 keys x 128 q] bf16
+    static constexpr int kOffBar = kOffDS + kKeys * kQTile * 2;
+    static constexpr int kBarKV = 0;
+    static constexpr int kBarFull = 1;                  // [kStages]
+    static constexpr int kBarEmpty = kBarFull + kStages;  // [kStages]
+    static constexpr int kBarS = kBarEmpty + kStages;
+    static constexpr int kBarP = kBarS + 1;
+    static constexpr int kBarDQ = kBarP + 1;
+    static constexpr int kBarDQUsed = kBarDQ + 1;
+    static constexpr int kBarDSFree = kBarDQUsed + 1;
+    static constexpr int kBarDKV = kBarDSFree + 1;
+    static constexpr int kBarDrain = kBarDKV + 1;
+    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kAlloc = kBytes + 1024;
+    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+    static_assert(kTDV + 2 * D <= kTmemCols, "TMEM budget");
+};
+
+__device__ __forceinline__ uint32_t sw128_offset(int row, int chunk)
+{
+    return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const float *__restrict__ lse, const float *__restrict__ dvec, float *__restrict__ dqacc,
+                    __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
+                    const int32_t *__restrict__ key_lens, int H, int N, int n_tiles, int num_bh, float scale,
+                    float scale_log2, int causal)
+{
+    using L = BwdSmem<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t s_base = smem_addr(smem);
+    const uint32_t sK = s_base + L::kOffK, sV = s_base + L::kOffV, sDS = s_base + L::kOffDS;
+    auto sQ = [&](int st) -> uint32_t { return s_base + L::kOffRing + st * 2 * L::kTileBytes; };
+    auto sDO = [&](int st) -> uint32_t { return sQ(st) + L::kTileBytes; };
+    auto bar = [&](int i) -> uint32_t { return s_base + L::kOffBar + 8 * i; };
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5;
+    // Key tiles in ascending order (the first ones see the most query tiles
+    // when causal), all heads of one key tile together.
+    const int bh = blockIdx.x % num_bh;
+    const int kt = static_cast<int>(blockIdx.x / num_bh);
+    const int b = bh / H, h = bh % H;
+    int kv_len = N;
+    if (key_lens != nullptr) kv_len = min(max(key_lens[b], 0), N);
+    const int k0 = kt * kKeys;
+    const int i_first = (causal && k0 < kv_len) ? kt : 0;
+    const int n_q = k0 < kv_len ? n_tiles - i_first : 0;  // query tiles this key tile meets
+
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::kBarKV), 1);
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(bar(L::kBarFull + s), 1);
+            mbar_init(bar(L::kBarEmpty + s), 1);
+        }
+        mbar_init(bar(L::kBarS), 1);
+        mbar_init(bar(L::kBarP), 4 * 32);
+        mbar_init(bar(L::kBarDQ), 1);
+        mbar_init(bar(L::kBarDQUsed), 4 * 32);
+        mbar_init(bar(L::kBarDSFree), 1);
+        mbar_init(bar(L::kBarDKV), 1);
+        mbar_init(bar(L::kBarDrain), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    auto wait_warp = [&](uint32_t b_addr, uint32_t parity, int site) -> bool {
+        return __all_sync(0xffffffffu, wait_bounded(b_addr, parity, abort_flag, site, &g_sdp18_bwd_error));
+    };
+
+    if (warp == kTmaWarp) {
+        // ------------------------------------------------------------ producer
+        if (n_q > 0) {
+            mbar_arrive_expect_tx_one(bar(L::kBarKV), 2 * L::kTileBytes);
+            for (int cb = 0; cb < D / 64; ++cb) {
+                tma_load_4d_one(sK + cb * 128 * 128, &tm_k, bar(L::kBarKV), cb * 64, k0, h, b);
+                tma_load_4d_one(sV + cb * 128 * 128, &tm_v, bar(L::kBarKV), cb * 64, k0, h, b);
+            }
+            int issued = 0;
+            for (int ii = 0; ii < n_q; ++ii) {
+                const int st = ii % L::kStages;
+                if (!wait_warp(bar(L::kBarEmpty + st), ((ii / L::kStages) & 1) ^ 1, 20)) break;
+                const int q0 = (i_first + ii) * kQTile;
+                mbar_arrive_expect_tx_one(bar(L::kBarFull + st), 2 * L::kTileBytes);
+                for (int cb = 0; cb < D / 64; ++cb) {
+                    tma_load_4d_one(sQ(st) + cb * 128 * 128, &tm_q, bar(L::kBarFull + st), cb * 64, q0, h, b);
+                    tma_load_4d_one(sDO(st) + cb * 128 * 128, &tm_do, bar(L::kBarFull + st), cb * 64, q0, h, b);
+                }
+                ++issued;
+            }
+            wait_drain(bar(L::kBarKV), 0);
+            for (int i = max(0, issued - L::kStages); i < issued; ++i)
+                wait_drain(bar(L::kBarFull + i % L::kStages), (i / L::kStages) & 1);
+        }
+    } else if (warp == kMmaWarp) {
+        // ------------------------------------------------------------ MMA issuer
+        if (n_q > 0) {
+            const uint32_t tm = __shfl_sync(0xffffffffu, tmem, 0);
+            constexpr uint32_t kIdS = idesc_bf16_f32_mn(kKeys, kQTile, false, false);  // S^T, dP^T
+            constexpr uint32_t kIdKV = idesc_bf16_f32_mn(kKeys, D, false, true);       // dV, dK
+            constexpr uint32_t kIdQ = idesc_bf16_f32_mn(kQTile, D, true, true);        // dQ
+            bool ok = wait_warp(bar(L::kBarKV), 0, 21);
+            for (int ii = 0; ii < n_q && ok; ++ii) {
+                const int st = ii % L::kStages;
+                ok = wait_warp(bar(L::kBarFull + st), (ii / L::kStages) & 1, 22);
+                // dQ_{i-1} sits in the dP^T columns until the compute warps read it.
+                if (ok && ii > 0) ok = wait_warp(bar(L::kBarDQUsed), (ii - 1) & 1, 23);
+                if (!ok) break;
+                tc_fence_after();
+                // S^T = K Q_i^T and dP^T = V dO_i^T (keys x queries, K = D).
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+                    mma_bf16_ss_one(tm + kTS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ(st) + off, 16, 1024),
+                                    kIdS, kk > 0 ? 1u : 0u);
+                }
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+                    mma_bf16_ss_one(tm + kTDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO(st) + off, 16, 1024),
+                                    kIdS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit_one(bar(L::kBarS));
+                ok = wait_warp(bar(L::kBarP), ii & 1, 24);
+                if (!ok) break;
+                tc_fence_after();
+                // dV += P^T dO_i: A = P^T from TMEM (16 queries = 8 packed columns per
+                // step), B = dO_i query-major (N = D).
+#pragma unroll
+                for (int kk = 0; kk < kQTile / 16; ++kk)
+                    mma_bf16_ts_one(tm + kTDV, tm + kTS + kk * 8, sdesc_sw128(sDO(st) + kk * 16 * 128, 128 * 128, 1024),
+                                    kIdKV, (ii > 0 || kk > 0) ? 1u : 0u);
+                // dK += dS^T Q_i: A = dS^T (keys x queries, K-major), B = Q_i query-major.
+#pragma unroll
+                for (int kk = 0; kk < kQTile / 16; ++kk)
+                    mma_bf16_ss_one(tm + kTDV + D, sdesc_sw128(sDS + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024),
+                                    sdesc_sw128(sQ(st) + kk * 16 * 128, 128 * 128, 1024), kIdKV,
+                                    (ii > 0 || kk > 0) ? 1u : 0u);
+                // dQ_i = dS K: A = dS^T read query-major (M = queries), B = K key-major (N = D).
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; ++kk)
+                    mma_bf16_ss_one(tm + kTDP, sdesc_sw128(sDS + kk * 16 * 128, 128 * 128, 1024),
+                                    sdesc_sw128(sK + kk * 16 * 128, 128 * 128, 1024), kIdQ, kk > 0 ? 1u : 0u);
+                mma_commit_one(bar(L::kBarDQ));
+                mma_commit_one(bar(L::kBarDSFree));
+                mma_commit_one(bar(L::kBarEmpty + st));
+            }
+            if (ok) mma_commit_one(bar(L::kBarDKV));
+            mma_commit_one(bar(L::kBarDrain));
+            wait_drain(bar(L::kBarDrain), 0);
+        }
+    } else {
+        // ------------------------------------------------------------ key rows
+        const int r = threadIdx.x;  // key row == TMEM lane
+        const int kj = k0 + r;
+        const bool key_ok = kj < kv_len;
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        bool ok = true;
+        for (int ii = 0; ii < n_q && ok; ++ii) {
+            const int q0 = (i_first + ii) * kQTile;
+            if (!wait_warp(bar(L::kBarS), ii & 1, 25)) {
+                ok = false;
+                break;
+            }
+            if (ii > 0 && !wait_warp(bar(L::kBarDSFree), (ii - 1) & 1, 26)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // 32 query columns at a time: P^T = exp2(S^T * scale*log2e - lse),
+            // dS^T = P^T (dP^T - D); P^T (bf16) over S^T's first 64 columns,
+            // dS^T (bf16) into shared memory (swizzled, keys x queries).
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                // Lane l fetches the statistics of query column 32c + l; every
+                // lane then reads all 32 by shuffles.  Columns past N or rows
+                // with no visible key (lse = -inf) get lse = +inf: P = 0.
+                float my_l2 = INFINITY, my_d = 0.f;
+                {
+                    const int q = q0 + 32 * c + (threadIdx.x & 31);
+                    if (q < N) {
+                        const float v = lse[static_cast<int64_t>(bh) * N + q];
+                        if (v > -INFINITY) my_l2 = v * kLog2e;
+                        my_d = dvec[static_cast<int64_t>(bh) * N + q];
+                    }
+                }
+                uint32_t sv[32], dpv[32];
+                tmem_ld32(t_lane + kTS + 32 * c, sv);
+                tmem_ld32(t_lane + kTDP + 32 * c, dpv);
+                tmem_ld_wait_only();
+                reg_fence(sv);
+                reg_fence(dpv);
+                uint32_t pk[16], dk16[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float p2[2], ds2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int col = 2 * e + u;
+                        const float l2 = __shfl_sync(0xffffffffu, my_l2, col);
+                        const float dd = __shfl_sync(0xffffffffu, my_d, col);
+                        const bool vis = key_ok && (!causal || q0 + 32 * c + col >= kj);
+                        const float p = vis ? ex2(fmaf(__uint_as_float(sv[col]), scale_log2, -l2)) : 0.f;
+                        p2[u] = p;
+                        ds2[u] = p * (__uint_as_float(dpv[col]) - dd);
+                    }
+                    pk[e] = pack_bf16x2(p2[0], p2[1]);
+                    dk16[e] = pack_bf16x2(ds2[0], ds2[1]);
+                }
+                tmem_st16(t_lane + kTS + 16 * c, pk);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c16 = 4 * c + u;  // 16-byte chunk of the 256-byte dS^T row
+                    st_shared_v4(sDS + (c16 >> 3) * (128 * 128) + sw128_offset(r, c16 & 7), dk16[4 * u],
+                                 dk16[4 * u + 1], dk16[4 * u + 2], dk16[4 * u + 3]);
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarP));
+            // dQ_i (queries in TMEM lanes) -> scale * dQ_i added into the accumulator.
+            if (!wait_warp(bar(L::kBarDQ), ii & 1, 27)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const int q = q0 + r;
+            float *dst = dqacc + (static_cast<int64_t>(bh) * N + q) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(t_lane + kTDP + 32 * c, o);
+                tmem_ld_wait(o);
+                if (q < N) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        red_add_v4(dst + 32 * c + 4 * e, scale * __uint_as_float(o[4 * e]),
+                                   scale * __uint_as_float(o[4 * e + 1]), scale * __uint_as_float(o[4 * e + 2]),
+                                   scale * __uint_as_float(o[4 * e + 3]));
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarDQUsed));
+        }
+        // ------------------------------------------------------------ dK, dV
+        // Warp-uniform: TMEM loads are collective; only the stores depend on
+        // the row.
+        const bool have = ok && n_q > 0 && wait_warp(bar(L::kBarDKV), 0, 28);
+        if (have) tc_fence_after();
+        if (ok) {
+            __nv_bfloat16 *pdv = dv + (static_cast<int64_t>(bh) * N + kj) * D;
+            __nv_bfloat16 *pdk = dk + (static_cast<int64_t>(bh) * N + kj) * D;
+#pragma unroll 1
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t a[32], g[32];
+                if (have) {
+                    tmem_ld32(t_lane + kTDV + 32 * c, a);
+                    tmem_ld32(t_lane + kTDV + D + 32 * c, g);
+                    tmem_ld_wait_only();
+                    reg_fence(a);
+                    reg_fence(g);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) a[e] = g[e] = 0u;
+                }
+                if (kj < N) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint4 wv, wk;
+                        wv.x = pack_bf16x2(__uint_as_float(a[8 * u + 0]), __uint_as_float(a[8 * u + 1]));
+                        wv.y = pack_bf16x2(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3]));
+                        wv.z = pack_bf16x2(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5]));
+                        wv.w = pack_bf16x2(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7]));
+                        wk.x = pack_bf16x2(scale * __uint_as_float(g[8 * u + 0]), scale * __uint_as_float(g[8 * u + 1]));
+                        wk.y = pack_bf16x2(scale * __uint_as_float(g[8 * u + 2]), scale * __uint_as_float(g[8 * u + 3]));
+                        wk.z = pack_bf16x2(scale * __uint_as_float(g[8 * u + 4]), scale * __uint_as_float(g[8 * u + 5]));
+                        wk.w = pack_bf16x2(scale * __uint_as_float(g[8 * u + 6]), scale * __uint_as_float(g[8 * u + 7]));
+                        *reinterpret_cast<uint4 *>(pdv + 32 * c + 8 * u) = wv;
+                        *reinterpret_cast<uint4 *>(pdk + 32 * c + 8 * u) = wk;
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+    }
+
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// D_i = dO_i . O_i (fp32) and dQ accumulator rows cleared; D/8 threads per row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prepare(const __nv_bfloat16 *__restrict__ out,
+                                                   const __nv_bfloat16 *__restrict__ dout, float *__restrict__ dvec,
+                                                   float *__restrict__ dqacc, int64_t rows)
+{
+    constexpr int kSeg = D / 8;
+    const int64_t row = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) / kSeg;
+    const int seg = threadIdx.x % kSeg;
+    float acc = 0.f;
+    if (row < rows) {
+        const uint4 o = *reinterpret_cast<const uint4 *>(out + row * D + seg * 8);
+        const uint4 g = *reinterpret_cast<const uint4 *>(dout + row * D + seg * 8);
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            acc = fmaf(__uint_as_float(ow[i] << 16), __uint_as_float(gw[i] << 16), acc);
+            acc = fmaf(__uint_as_float(ow[i] & 0xFFFF0000u), __uint_as_float(gw[i] & 0xFFFF0000u), acc);
+        }
+        float4 *z = reinterpret_cast<float4 *>(dqacc + row * D + seg * 8);
+        z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+        z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = kSeg / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (row < rows && seg == 0) dvec[row] = acc;
+}
+
+__global__ void __launch_bounds__(256) bwd_finish(const float *__restrict__ dqacc, __nv_bfloat16 *__restrict__ dq,
+                                                  int64_t n4)
+{
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
+    if (i >= n4) return;
+    const float4 v = reinterpret_cast<const float4 *>(dqacc)[i];
+    uint2 w;
+    w.x = pack_bf16x2(v.x, v.y);
+    w.y = pack_bf16x2(v.z, v.w);
+    reinterpret_cast<uint2 *>(dq)[i] = w;
+}
+
+template <int D>
+int launch_bwd(const BwdLaunch &a)
+{
+    using L = BwdSmem<D>;
+    static int configured_device = -1;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (configured_device != dev) {
+        if (cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
+            cudaSuccess)
+            return -1;
+        configured_device = dev;
+    }
+    const int64_t rows = static_cast<int64_t>(a.B) * a.H * a.N;
+    const int64_t seg_threads = rows * (D / 8);
+    bwd_prepare<D><<<static_cast<unsigned>((seg_threads + 255) / 256), 256, 0, a.stream>>>(
+        static_cast<const __nv_bfloat16 *>(a.out), static_cast<const __nv_bfloat16 *>(a.dout), a.dvec, a.dqacc,
+        rows);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    const int n_tiles = (a.N + 127) / 128;
+    const int num_bh = a.B * a.H;
+    attn_bwd_kernel<D><<<static_cast<unsigned>(n_tiles) * num_bh, kThreads, L::kAlloc, a.stream>>>(
+        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, a.lse, a.dvec, a.dqacc, static_cast<__nv_bfloat16 *>(a.dk),
+        static_cast<__nv_bfloat16 *>(a.dv), a.key_lens, a.H, a.N, n_tiles, num_bh, a.scale,
+        a.scale * kLog2e, a.causal);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    const int64_t n4 = rows * D / 4;
+    bwd_finish<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, a.stream>>>(a.dqacc,
+                                                                            static_cast<__nv_bfloat16 *>(a.dq), n4);
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+int attn_bwd_launch(const BwdLaunch &a)
+{
+    if (a.d == 64) return launch_bwd<64>(a);
+    if (a.d == 128) return launch_bwd<128>(a);
+    return -2;
+}
+
+int read_and_clear_bwd_error(int *value)
+{
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_sdp18_bwd_error, sizeof(int)) != cudaSuccess) return -1;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_sdp18_bwd_error, &zero, sizeof(int)) != cudaSuccess) return -1;
+    }
+    *value = v;
+    return 0;
+}
+
+}  // namespace sdp18

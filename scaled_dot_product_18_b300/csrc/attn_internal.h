@@ -45,7 +45,26 @@ struct DecodeLaunch {
 // 0 on success, -1 on a CUDA error, -2 for an unsupported head dimension.
 int attn_decode_launch(const DecodeLaunch &a);
 
+// Backward (dQ, dK, dV).
+struct BwdLaunch {
+    const CUtensorMap *tm_q, *tm_k, *tm_v, *tm_do;  // 4-D maps {d, N, H, B} bf16
+    const void *out, *dout;                         // bf16 [B*H*N, d] (contiguous)
+    const float *lse;                               // [B*H*N] natural log, from the forward
+    float *dvec;                                    // [B*H*N] workspace: dO . O
+    float *dqacc;                                   // [B*H*N, d] workspace: fp32 dQ accumulator
+    void *dq, *dk, *dv;                             // bf16 [B*H*N, d]
+    const int32_t *key_lens;
+    int B, H, N, d;
+    float scale;
+    int causal;
+    cudaStream_t stream;
+};
+// 0 on success, -1 on a CUDA error, -2 for an unsupported head dimension.
+int attn_bwd_launch(const BwdLaunch &a);
+
 // Reads the device error word of the current device and clears it.
 int read_and_clear_device_error(int *value);
+// Same for the word the backward kernel writes.
+int read_and_clear_bwd_error(int *value);
 
 }  // namespace sdp18

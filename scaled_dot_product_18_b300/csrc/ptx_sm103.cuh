@@ -329,6 +329,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool b_mn_ma
            | (static_cast<uint32_t>(M >> 4) << 24); // M / 16
 }
 
+// Same with either operand MN-major (A's M or B's N dimension contiguous).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_mn(int M, int N, bool a_mn_major, bool b_mn_major)
+{
+    return idesc_bf16_f32(M, N, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
+}
+
 // 32 lanes x 32 columns of 32-bit TMEM -> 32 registers per thread (thread t
 // of the warp gets lane base+t).  Followed by tmem_ld_wait before use.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])

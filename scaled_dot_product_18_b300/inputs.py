@@ -38,7 +38,7 @@ GOLDEN = np.uint64(0x9E3779B97F4A7C15)
 _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
-STREAM_Q, STREAM_K, STREAM_V, STREAM_KEYLEN = 0, 1, 2, 3
+STREAM_Q, STREAM_K, STREAM_V, STREAM_KEYLEN, STREAM_DOUT = 0, 1, 2, 3, 4
 
 _CHUNK = 1 << 19  # Box-Muller pairs per vectorised block (keeps temporaries small)
 _THREADS = max(1, min(16, os.cpu_count() or 1))
@@ -218,6 +218,13 @@ def make_inputs(w: Workload, seed: int | None = None) -> HostInputs:
     v = make_tensor_bits(s, STREAM_V, shape, w.amplitude)
     kl = make_key_lens(s, w.B, *w.key_len_range) if w.key_len_range else None
     return HostInputs(q, k, v, kl)
+
+
+def make_dout(w: Workload, seed: int | None = None) -> np.ndarray:
+    """bf16 bits of the loss gradient dO [B, H, N, d] for the backward: N(0,1),
+    its own stream of the workload's seed."""
+    s = w.seed if seed is None else seed
+    return make_tensor_bits(s, STREAM_DOUT, (w.B, w.H, w.N, w.d))
 
 
 @dataclasses.dataclass(frozen=True)

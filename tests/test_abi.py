@@ -30,14 +30,15 @@ def declared_functions():
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert {"attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_workspace_size", "attn_mha_fwd",
-            "attn_mha_workspace_size", "attn_check_device", "attn_status_str", "attn_abi_version"} <= names
+            "attn_mha_workspace_size", "attn_bwd", "attn_bwd_workspace_size", "attn_check_device", "attn_status_str",
+            "attn_abi_version"} <= names
     assert names == set(sdp.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
 
 
 def test_abi_version_and_status_strings(lib):
-    assert sdp.attn_abi_version() == 3
+    assert sdp.attn_abi_version() == 4
     for code in (0, -1, -2, -3, -4, -5):
         assert sdp.attn_status_str(code).startswith("ATTN_")
     assert sdp.attn_status_str(7) == "unknown attn_status"
@@ -170,3 +171,45 @@ def test_oracle_not_imported_by_product():
                 txt = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in txt and "from oracle" not in txt, fn
                 assert "attn_oracle" not in txt, fn
+
+
+def test_bwd_workspace_size(lib):
+    # fp32 dQ accumulator plus the fp32 D vector, each rounded up to 256 bytes
+    assert sdp.attn_bwd_workspace_size(2, 3, 5, 64) == 2 * 3 * 5 * 64 * 4 + 256
+    assert sdp.attn_bwd_workspace_size(1, 32, 16384, 128) == 32 * 16384 * (128 + 1) * 4
+    assert sdp.attn_bwd_workspace_size(1, 1, 8, 96) == 0
+    assert sdp.attn_bwd_workspace_size(0, 1, 8, 64) == 0
+
+
+@pytest.mark.parametrize("args,want", [
+    (dict(d=96), sdp.ATTN_EUNSUPPORTED),
+    (dict(B=-1), sdp.ATTN_EINVAL),
+    (dict(N=-1), sdp.ATTN_EINVAL),
+    (dict(scale=0.0), sdp.ATTN_EINVAL),
+    (dict(scale=float("nan")), sdp.ATTN_EINVAL),
+    (dict(q=None), sdp.ATTN_EINVAL),
+    (dict(out=None), sdp.ATTN_EINVAL),
+    (dict(dout=None), sdp.ATTN_EINVAL),
+    (dict(lse=None), sdp.ATTN_EINVAL),
+    (dict(dq=None), sdp.ATTN_EINVAL),
+    (dict(dv=None), sdp.ATTN_EINVAL),
+    (dict(ws=None), sdp.ATTN_EINVAL),
+    (dict(ws_bytes=64), sdp.ATTN_EINVAL),
+    (dict(k=P + 8), sdp.ATTN_EALIGN),
+    (dict(dout=P + 2), sdp.ATTN_EALIGN),
+    (dict(dk=P + 4), sdp.ATTN_EALIGN),
+    (dict(lse=P + 2), sdp.ATTN_EALIGN),
+    (dict(ws=P + 8), sdp.ATTN_EALIGN),
+    (dict(key_lens=P + 1), sdp.ATTN_EALIGN),
+    (dict(B=1 << 16, H=1 << 15), sdp.ATTN_EINVAL),
+    (dict(B=0, q=None, ws=None), sdp.ATTN_OK),
+    (dict(N=0), sdp.ATTN_OK),
+])
+def test_bwd_host_side_rejections(lib, args, want):
+    a = dict(q=P, k=P, v=P, out=P, dout=P, lse=P, dq=P, dk=P, dv=P, B=2, H=3, N=5, d=64, scale=0.125, causal=1,
+             key_lens=None, ws=P, ws_bytes=1 << 30, stream=None)
+    a.update(args)
+    st = lib.attn_bwd(a["q"], a["k"], a["v"], a["out"], a["dout"], a["lse"], a["dq"], a["dk"], a["dv"], a["B"],
+                      a["H"], a["N"], a["d"], a["scale"], a["causal"], a["key_lens"], a["ws"], a["ws_bytes"],
+                      a["stream"])
+    assert st == want, (args, st)

@@ -503,6 +503,30 @@ def test_backward_sampled_matches_literal():
             np.testing.assert_allclose(sv, dV[b, h, rows], atol=1e-11)
 
 
+def test_backward_with_stored_output_identity():
+    # D from dO . O (O the exact forward output) equals D from P and dP, so
+    # passing the exact output changes nothing; a perturbed output moves dQ
+    # and dK (through dS) but never dV.
+    r = np.random.default_rng(64)
+    B, H, N, d = 2, 2, 9, 4
+    q, k, v, g = (r.standard_normal((B, H, N, d)) for _ in range(4))
+    kl = np.array([7, 9], dtype=np.int32)
+    for causal in (False, True):
+        ref = oracle.attention_backward_literal(q, k, v, g, 0.6, causal, kl)
+        O, _, _ = oracle.attention_literal(q, k, v, 0.6, causal, kl)
+        same = oracle.attention_backward_literal(q, k, v, g, 0.6, causal, kl, out=O)
+        for a, b in zip(ref, same):
+            np.testing.assert_allclose(a, b, atol=1e-12)
+        moved = oracle.attention_backward_literal(q, k, v, g, 0.6, causal, kl, out=O + 0.01)
+        np.testing.assert_array_equal(moved[2], ref[2])
+        assert np.abs(moved[0] - ref[0]).max() > 1e-4 and np.abs(moved[1] - ref[1]).max() > 1e-4
+        rows = [0, 3, 8]
+        sm = oracle.attention_backward_sampled(q, k, v, g, 0.6, causal, kl, heads=[(1, 0)], q_rows=rows,
+                                               k_rows=rows, out=O + 0.01)
+        for got, want in zip(sm[(1, 0)], moved):
+            np.testing.assert_allclose(got, want[1, 0, rows], atol=1e-11)
+
+
 def test_backward_uniform_attention_closed_form():
     # Q = 0: P is uniform over the visible keys, so dV_j = (1/n) sum over the
     # rows that see key j of dO_i, computed here with explicit counts.
