@@ -289,9 +289,30 @@ attn_status attn_decode(const void *q, const void *k_cache, const void *v_cache,
 size_t attn_bwd_workspace_size(int B, int H, int N, int d)
 {
     if (B <= 0 || H <= 0 || N <= 0 || (d != 64 && d != 128)) return 0;
-    const size_t rows = static_cast<size_t>(B) * H * N;
-    return round256(rows * d * sizeof(float)) + round256(rows * sizeof(float));
+    const size_t bh = static_cast<size_t>(B) * H;
+    const size_t n_pad = (static_cast<size_t>(N) + 127) / 128 * 128;
+    // fp32 dQ accumulator [B*H*N, d], then lse*log2e and D per padded query row
+    return round256(bh * N * d * sizeof(float)) + round256(2 * bh * n_pad * sizeof(float));
 }
+
+namespace {
+
+// 3-D view {d, N, B*H} of the fp32 dQ accumulator with 32 x 32 boxes (128-byte
+// rows, 128-byte swizzle): the target of the backward's TMA reductions.
+bool make_dq_map(CUtensorMap *m, float *base, int64_t BH, int N, int d)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
 
 attn_status attn_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
                      void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal,
@@ -318,16 +339,20 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *ou
         !make_map(&tdo, dout, B, H, N, d, st))
         return ATTN_ECUDA;
     const size_t rows = static_cast<size_t>(bh) * N;
+    float *dqacc = static_cast<float *>(workspace);
+    CUtensorMap tdq;
+    if (!make_dq_map(&tdq, dqacc, bh, N, d)) return ATTN_ECUDA;
     sdp18::BwdLaunch a{};
     a.tm_q = &tq;
     a.tm_k = &tk;
     a.tm_v = &tv;
     a.tm_do = &tdo;
+    a.tm_dq = &tdq;
     a.out = out;
     a.dout = dout;
     a.lse = lse;
-    a.dqacc = static_cast<float *>(workspace);
-    a.dvec = reinterpret_cast<float *>(static_cast<char *>(workspace) + round256(rows * d * sizeof(float)));
+    a.dqacc = dqacc;
+    a.stats = reinterpret_cast<float *>(static_cast<char *>(workspace) + round256(rows * d * sizeof(float)));
     a.dq = dq;
     a.dk = dk;
     a.dv = dv;

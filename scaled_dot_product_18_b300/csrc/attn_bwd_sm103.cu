@@ -11,20 +11,26 @@
 // One CTA owns a 128-key tile of one (batch, head) and walks the query tiles
 // that can see it (all of them, or those at or after the diagonal when
 // causal).  Per query tile, in tensor memory (512 columns):
-//   S^T = K Q_i^T          columns   0..127  (keys in TMEM lanes)
+//   S^T = K Q_i^T          columns   0..127  (keys in TMEM lanes, queries in columns)
 //   dP^T = V dO_i^T        columns 128..255
-//   P^T -> bf16 over the first 64 columns of S^T (A operand of dV += P^T dO_i)
+//   P^T -> bf16 packed over columns 0..31 and 64..95 of S^T (each half of
+//          the compute warps overwrites only columns it has read), the A
+//          operand of dV += P^T dO_i
 //   dS^T -> bf16 in shared memory (A operand of dK += dS^T Q_i, and, read
 //          query-major, of dQ_i = dS K, which lands in the dP^T columns)
 //   dV, dK accumulate in columns 256.. across the query tiles.
-// dQ_i is added (times scale) to an fp32 accumulator in global memory with
-// vector reductions; a pre-pass computes D and clears the accumulator, a
-// post-pass converts it to bf16.
+// The MMA order per tile is S, dP, dV, dK, dQ: S^T is issued as soon as the
+// previous tile's dQ MMAs are queued, the compute warps turn S^T into P while
+// dP^T is being computed, and dS while dV is; dQ_i is added (times scale) to
+// an fp32 accumulator in global memory by TMA reductions staged through each
+// warp's own part of the dS^T buffer.  A pre-pass computes D, the scaled LSE
+// and clears the accumulator, a post-pass converts it to bf16.
 //
-//   warps 0-3  key row r = thread (TMEM lane r): P^T, dS^T, dQ reduction,
-//              the dK / dV epilogue.
-//   warp 4     TMA producer: K, V once; Q_i, dO_i through a 2-stage ring.
-//   warp 5     allocates TMEM and issues the five MMAs of each query tile.
+//   warps 0-7  compute: warp w serves key rows 32 (w % 4) .. +31 (its TMEM
+//              lanes) and query columns 64 (w / 4) .. +63: P^T, dS^T; then
+//              dQ rows 32 (w % 4) .. of head-dim half w / 4; then dK and dV.
+//   warp 8     TMA producer: K, V once; (Q_i, dO_i, LSE, D) through a 2-stage ring.
+//   warp 9     allocates TMEM and issues the five MMAs of each query tile.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -44,37 +50,41 @@ namespace {
 
 constexpr int kKeys = 128;    // keys per CTA
 constexpr int kQTile = 128;   // queries per step
-constexpr int kThreads = 192;
-constexpr int kTmaWarp = 4;
-constexpr int kMmaWarp = 5;
+constexpr int kCompute = 8;   // compute warps
+constexpr int kThreads = (kCompute + 2) * 32;
+constexpr int kTmaWarp = kCompute;
+constexpr int kMmaWarp = kCompute + 1;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTS = 0, kTDP = 128, kTDV = 256;  // dK at kTDV + D
 constexpr float kLog2e = 1.4426950408889634f;
+enum : int { kErrSmemAlign = 4 };
 
 template <int D>
 struct BwdSmem {
     static constexpr int kTileBytes = 128 * D * 2;  // one [128 x D] bf16 tile
-    static constexpr int kStages = 2;               // (Q_i, dO_i) stages
+    static constexpr int kStages = 2;               // (Q_i, dO_i, stats) stages
     static constexpr int kOffK = 0;
     static constexpr int kOffV = kOffK + kTileBytes;
     static constexpr int kOffRing = kOffV + kTileBytes;  // stage s: Q at +0, dO at +kTileBytes
     static constexpr int kOffDS = kOffRing + kStages * 2 * kTileBytes;  // [128 keys x 128 q] bf16
-    static constexpr int kOffBar = kOffDS + kKeys * kQTile * 2;
+    static constexpr int kOffStat = kOffDS + kKeys * kQTile * 2;      // stage s: lse*log2e [128], D [128]
+    static constexpr int kStatBytes = 2 * kQTile * 4;
+    static constexpr int kOffBar = kOffStat + kStages * kStatBytes;
     static constexpr int kBarKV = 0;
-    static constexpr int kBarFull = 1;                  // [kStages]
+    static constexpr int kBarFull = 1;                    // [kStages]
     static constexpr int kBarEmpty = kBarFull + kStages;  // [kStages]
     static constexpr int kBarS = kBarEmpty + kStages;
-    static constexpr int kBarP = kBarS + 1;
-    static constexpr int kBarDQ = kBarP + 1;
+    static constexpr int kBarDP = kBarS + 1;
+    static constexpr int kBarP = kBarDP + 1;
+    static constexpr int kBarDS = kBarP + 1;
+    static constexpr int kBarDQ = kBarDS + 1;
     static constexpr int kBarDQUsed = kBarDQ + 1;
-    static constexpr int kBarDSFree = kBarDQUsed + 1;
-    static constexpr int kBarDKV = kBarDSFree + 1;
+    static constexpr int kBarDKV = kBarDQUsed + 1;
     static constexpr int kBarDrain = kBarDKV + 1;
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;
     static constexpr int kBytes = kOffMisc + 16;
-    static constexpr int kAlloc = kBytes + 1024;
-    static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+    static_assert(kBytes <= 227 * 1024, "shared memory budget");
     static_assert(kTDV + 2 * D <= kTmemCols, "TMEM budget");
 };
 
@@ -83,33 +93,39 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk)
     return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d)
+__device__ __forceinline__ void ld_shared_v4f(uint32_t addr, float &a, float &b, float &c, float &d)
 {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
-                 : "memory");
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(a), "=f"(b), "=f"(c), "=f"(d) : "r"(addr));
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const float *__restrict__ lse, const float *__restrict__ dvec, float *__restrict__ dqacc,
+                    const __grid_constant__ CUtensorMap tm_dq, const float *__restrict__ stats,
                     __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
                     const int32_t *__restrict__ key_lens, int H, int N, int n_tiles, int num_bh, float scale,
                     float scale_log2, int causal)
 {
     using L = BwdSmem<D>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // The tiles are 128-byte swizzled and need a 1024-byte aligned base.  The
+    // check is uniform over the CTA, before any barrier or TMEM is touched.
+    extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t s_base = smem_addr(smem);
+    if (s_base & 1023u) {
+        if (threadIdx.x == 0) atomicOr(&g_sdp18_bwd_error, kErrSmemAlign);
+        return;
+    }
     const uint32_t sK = s_base + L::kOffK, sV = s_base + L::kOffV, sDS = s_base + L::kOffDS;
     auto sQ = [&](int st) -> uint32_t { return s_base + L::kOffRing + st * 2 * L::kTileBytes; };
     auto sDO = [&](int st) -> uint32_t { return sQ(st) + L::kTileBytes; };
+    auto sStat = [&](int st) -> uint32_t { return s_base + L::kOffStat + st * L::kStatBytes; };
     auto bar = [&](int i) -> uint32_t { return s_base + L::kOffBar + 8 * i; };
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::kOffMisc);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     // Key tiles in ascending order (the first ones see the most query tiles
     // when causal), all heads of one key tile together.
     const int bh = blockIdx.x % num_bh;
@@ -120,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int k0 = kt * kKeys;
     const int i_first = (causal && k0 < kv_len) ? kt : 0;
     const int n_q = k0 < kv_len ? n_tiles - i_first : 0;  // query tiles this key tile meets
+    const int n_pad = n_tiles * kQTile;
 
     if (threadIdx.x == 0) {
         mbar_init(bar(L::kBarKV), 1);
@@ -128,10 +145,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::kBarEmpty + s), 1);
         }
         mbar_init(bar(L::kBarS), 1);
-        mbar_init(bar(L::kBarP), 4 * 32);
+        mbar_init(bar(L::kBarDP), 1);
+        mbar_init(bar(L::kBarP), kCompute * 32);
+        mbar_init(bar(L::kBarDS), kCompute * 32);
         mbar_init(bar(L::kBarDQ), 1);
-        mbar_init(bar(L::kBarDQUsed), 4 * 32);
-        mbar_init(bar(L::kBarDSFree), 1);
+        mbar_init(bar(L::kBarDQUsed), kCompute * 32);
         mbar_init(bar(L::kBarDKV), 1);
         mbar_init(bar(L::kBarDrain), 1);
         *abort_flag = 0;
@@ -157,16 +175,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_4d_one(sK + cb * 128 * 128, &tm_k, bar(L::kBarKV), cb * 64, k0, h, b);
                 tma_load_4d_one(sV + cb * 128 * 128, &tm_v, bar(L::kBarKV), cb * 64, k0, h, b);
             }
+            const float *lse2 = stats + static_cast<int64_t>(bh) * n_pad;
+            const float *dvec = stats + static_cast<int64_t>(num_bh) * n_pad + static_cast<int64_t>(bh) * n_pad;
             int issued = 0;
             for (int ii = 0; ii < n_q; ++ii) {
                 const int st = ii % L::kStages;
                 if (!wait_warp(bar(L::kBarEmpty + st), ((ii / L::kStages) & 1) ^ 1, 20)) break;
                 const int q0 = (i_first + ii) * kQTile;
-                mbar_arrive_expect_tx_one(bar(L::kBarFull + st), 2 * L::kTileBytes);
+                mbar_arrive_expect_tx_one(bar(L::kBarFull + st), 2 * L::kTileBytes + L::kStatBytes);
                 for (int cb = 0; cb < D / 64; ++cb) {
                     tma_load_4d_one(sQ(st) + cb * 128 * 128, &tm_q, bar(L::kBarFull + st), cb * 64, q0, h, b);
                     tma_load_4d_one(sDO(st) + cb * 128 * 128, &tm_do, bar(L::kBarFull + st), cb * 64, q0, h, b);
                 }
+                bulk_load_one(sStat(st), lse2 + q0, kQTile * 4, bar(L::kBarFull + st));
+                bulk_load_one(sStat(st) + kQTile * 4, dvec + q0, kQTile * 4, bar(L::kBarFull + st));
                 ++issued;
             }
             wait_drain(bar(L::kBarKV), 0);
@@ -184,33 +206,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int ii = 0; ii < n_q && ok; ++ii) {
                 const int st = ii % L::kStages;
                 ok = wait_warp(bar(L::kBarFull + st), (ii / L::kStages) & 1, 22);
-                // dQ_{i-1} sits in the dP^T columns until the compute warps read it.
-                if (ok && ii > 0) ok = wait_warp(bar(L::kBarDQUsed), (ii - 1) & 1, 23);
                 if (!ok) break;
                 tc_fence_after();
-                // S^T = K Q_i^T and dP^T = V dO_i^T (keys x queries, K = D).
+                // S^T = K Q_i^T (keys x queries, K = D).  The previous tile's P^T
+                // in these columns was consumed by its dV MMAs, queued earlier.
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
                     mma_bf16_ss_one(tm + kTS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sQ(st) + off, 16, 1024),
                                     kIdS, kk > 0 ? 1u : 0u);
                 }
+                mma_commit_one(bar(L::kBarS));
+                // dP^T = V dO_i^T overwrites dQ_{i-1}: wait until it has been read.
+                if (ii > 0 && !(ok = wait_warp(bar(L::kBarDQUsed), (ii - 1) & 1, 23))) break;
+                tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
                     mma_bf16_ss_one(tm + kTDP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO(st) + off, 16, 1024),
                                     kIdS, kk > 0 ? 1u : 0u);
                 }
-                mma_commit_one(bar(L::kBarS));
-                ok = wait_warp(bar(L::kBarP), ii & 1, 24);
-                if (!ok) break;
+                mma_commit_one(bar(L::kBarDP));
+                if (!(ok = wait_warp(bar(L::kBarP), ii & 1, 24))) break;
                 tc_fence_after();
-                // dV += P^T dO_i: A = P^T from TMEM (16 queries = 8 packed columns per
-                // step), B = dO_i query-major (N = D).
+                // dV += P^T dO_i: A = P^T from TMEM (16 queries = 8 packed
+                // columns per step; queries 64.. start at column 64), B = dO_i
+                // query-major (N = D).
 #pragma unroll
                 for (int kk = 0; kk < kQTile / 16; ++kk)
-                    mma_bf16_ts_one(tm + kTDV, tm + kTS + kk * 8, sdesc_sw128(sDO(st) + kk * 16 * 128, 128 * 128, 1024),
-                                    kIdKV, (ii > 0 || kk > 0) ? 1u : 0u);
+                    mma_bf16_ts_one(tm + kTDV, tm + kTS + (kk >> 2) * 64 + (kk & 3) * 8,
+                                    sdesc_sw128(sDO(st) + kk * 16 * 128, 128 * 128, 1024), kIdKV,
+                                    (ii > 0 || kk > 0) ? 1u : 0u);
+                if (!(ok = wait_warp(bar(L::kBarDS), ii & 1, 25))) break;
+                tc_fence_after();
                 // dK += dS^T Q_i: A = dS^T (keys x queries, K-major), B = Q_i query-major.
 #pragma unroll
                 for (int kk = 0; kk < kQTile / 16; ++kk)
@@ -223,7 +251,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16_ss_one(tm + kTDP, sdesc_sw128(sDS + kk * 16 * 128, 128 * 128, 1024),
                                     sdesc_sw128(sK + kk * 16 * 128, 128 * 128, 1024), kIdQ, kk > 0 ? 1u : 0u);
                 mma_commit_one(bar(L::kBarDQ));
-                mma_commit_one(bar(L::kBarDSFree));
                 mma_commit_one(bar(L::kBarEmpty + st));
             }
             if (ok) mma_commit_one(bar(L::kBarDKV));
@@ -231,119 +258,156 @@ __global__ void __launch_bounds__(kThreads, 1)
             wait_drain(bar(L::kBarDrain), 0);
         }
     } else {
-        // ------------------------------------------------------------ key rows
-        const int r = threadIdx.x;  // key row == TMEM lane
+        // ------------------------------------------------------------ compute warps
+        const int g = warp & 3;   // TMEM lane quarter: key rows / dQ rows 32g..32g+31
+        const int hf = warp >> 2;  // query-column half (P, dS) and head-dim half (dQ, dK, dV)
+        const int r = 32 * g + lane;  // key row == TMEM lane
         const int kj = k0 + r;
         const bool key_ok = kj < kv_len;
-        const uint32_t t_lane = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const bool tail_keys = k0 + kKeys > kv_len;  // some key of this tile is hidden
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * g) << 16);
+        // This warp's 4 KB of the dS^T buffer (its key rows, its query half);
+        // between tiles it stages the warp's dQ boxes for the TMA reduction.
+        const uint32_t s_mine = sDS + hf * (128 * 128) + g * 4096;
         bool ok = true;
         for (int ii = 0; ii < n_q && ok; ++ii) {
+            const int st = ii % L::kStages;
             const int q0 = (i_first + ii) * kQTile;
-            if (!wait_warp(bar(L::kBarS), ii & 1, 25)) {
-                ok = false;
-                break;
-            }
-            if (ii > 0 && !wait_warp(bar(L::kBarDSFree), (ii - 1) & 1, 26)) {
+            const bool masked = tail_keys || (causal && q0 == k0);  // per-element visibility needed
+            if (!wait_warp(bar(L::kBarFull + st), (ii / L::kStages) & 1, 26) || !wait_warp(bar(L::kBarS), ii & 1, 27)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // 32 query columns at a time: P^T = exp2(S^T * scale*log2e - lse),
-            // dS^T = P^T (dP^T - D); P^T (bf16) over S^T's first 64 columns,
-            // dS^T (bf16) into shared memory (swizzled, keys x queries).
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                // Lane l fetches the statistics of query column 32c + l; every
-                // lane then reads all 32 by shuffles.  Columns past N or rows
-                // with no visible key (lse = -inf) get lse = +inf: P = 0.
-                float my_l2 = INFINITY, my_d = 0.f;
-                {
-                    const int q = q0 + 32 * c + (threadIdx.x & 31);
-                    if (q < N) {
-                        const float v = lse[static_cast<int64_t>(bh) * N + q];
-                        if (v > -INFINITY) my_l2 = v * kLog2e;
-                        my_d = dvec[static_cast<int64_t>(bh) * N + q];
-                    }
-                }
-                uint32_t sv[32], dpv[32];
-                tmem_ld32(t_lane + kTS + 32 * c, sv);
-                tmem_ld32(t_lane + kTDP + 32 * c, dpv);
+            // P^T = exp2(S^T * scale*log2e - lse*log2e) over this warp's 64
+            // query columns, kept in fp32 for dS and stored as bf16 over the
+            // first 32 of those columns.
+            float p[64];
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = 64 * hf + 32 * cc;  // first query column of the chunk
+                uint32_t sv[32];
+                tmem_ld32(t_lane + kTS + c0, sv);
+                float l2[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    ld_shared_v4f(sStat(st) + (c0 + 4 * e) * 4, l2[4 * e], l2[4 * e + 1], l2[4 * e + 2], l2[4 * e + 3]);
                 tmem_ld_wait_only();
                 reg_fence(sv);
-                reg_fence(dpv);
-                uint32_t pk[16], dk16[16];
+                if (!masked) {
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float p2[2], ds2[2];
+                    for (int e = 0; e < 32; ++e) p[32 * cc + e] = ex2(fmaf(__uint_as_float(sv[e]), scale_log2, -l2[e]));
+                } else {
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int col = 2 * e + u;
-                        const float l2 = __shfl_sync(0xffffffffu, my_l2, col);
-                        const float dd = __shfl_sync(0xffffffffu, my_d, col);
-                        const bool vis = key_ok && (!causal || q0 + 32 * c + col >= kj);
-                        const float p = vis ? ex2(fmaf(__uint_as_float(sv[col]), scale_log2, -l2)) : 0.f;
-                        p2[u] = p;
-                        ds2[u] = p * (__uint_as_float(dpv[col]) - dd);
+                    for (int e = 0; e < 32; ++e) {
+                        const bool vis = key_ok && (!causal || q0 + c0 + e >= kj);
+                        p[32 * cc + e] = vis ? ex2(fmaf(__uint_as_float(sv[e]), scale_log2, -l2[e])) : 0.f;
                     }
-                    pk[e] = pack_bf16x2(p2[0], p2[1]);
-                    dk16[e] = pack_bf16x2(ds2[0], ds2[1]);
                 }
-                tmem_st16(t_lane + kTS + 16 * c, pk);
+                uint32_t pk[16];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int c16 = 4 * c + u;  // 16-byte chunk of the 256-byte dS^T row
-                    st_shared_v4(sDS + (c16 >> 3) * (128 * 128) + sw128_offset(r, c16 & 7), dk16[4 * u],
-                                 dk16[4 * u + 1], dk16[4 * u + 2], dk16[4 * u + 3]);
-                }
+                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(p[32 * cc + 2 * e], p[32 * cc + 2 * e + 1]);
+                tmem_st16(t_lane + kTS + 64 * hf + 16 * cc, pk);
             }
             tmem_st_wait();
-            fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(L::kBarP));
-            // dQ_i (queries in TMEM lanes) -> scale * dQ_i added into the accumulator.
-            if (!wait_warp(bar(L::kBarDQ), ii & 1, 27)) {
+            // The warp's staging area held last tile's dQ boxes: wait until the
+            // TMA has read them before writing dS^T there.
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            if (!wait_warp(bar(L::kBarDP), ii & 1, 28)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const int q = q0 + r;
-            float *dst = dqacc + (static_cast<int64_t>(bh) * N + q) * D;
-#pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(t_lane + kTDP + 32 * c, o);
-                tmem_ld_wait(o);
-                if (q < N) {
+            // dS^T = P^T (dP^T - D) -> bf16, swizzled keys x queries in shared memory.
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        red_add_v4(dst + 32 * c + 4 * e, scale * __uint_as_float(o[4 * e]),
-                                   scale * __uint_as_float(o[4 * e + 1]), scale * __uint_as_float(o[4 * e + 2]),
-                                   scale * __uint_as_float(o[4 * e + 3]));
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c0 = 64 * hf + 32 * cc;
+                uint32_t dpv[32];
+                tmem_ld32(t_lane + kTDP + c0, dpv);
+                float dd[32];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    ld_shared_v4f(sStat(st) + kQTile * 4 + (c0 + 4 * e) * 4, dd[4 * e], dd[4 * e + 1], dd[4 * e + 2],
+                                  dd[4 * e + 3]);
+                tmem_ld_wait_only();
+                reg_fence(dpv);
+                uint32_t w[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack_bf16x2(p[32 * cc + 2 * e] * (__uint_as_float(dpv[2 * e]) - dd[2 * e]),
+                                       p[32 * cc + 2 * e + 1] * (__uint_as_float(dpv[2 * e + 1]) - dd[2 * e + 1]));
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int c16 = (c0 >> 3) + u - 8 * hf;  // 16-byte chunk within the half's 128-byte row
+                    st_shared_v4(s_mine + sw128_offset(lane, c16), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
                 }
             }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(L::kBarDS));
+            // dQ_i (queries in TMEM lanes): this warp's rows and head-dim half,
+            // times scale, added into the fp32 accumulator by TMA reductions.
+            if (!wait_warp(bar(L::kBarDQ), ii & 1, 29)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            constexpr int kDqChunks = D / 64;  // 32-column boxes per warp
+            uint32_t o[kDqChunks][32];
+#pragma unroll
+            for (int j = 0; j < kDqChunks; ++j) tmem_ld32(t_lane + kTDP + hf * (D / 2) + 32 * j, o[j]);
+            tmem_ld_wait_only();
+#pragma unroll
+            for (int j = 0; j < kDqChunks; ++j) reg_fence(o[j]);
             tc_fence_before();
             mbar_arrive(bar(L::kBarDQUsed));
+            const int qrow = q0 + 32 * g;
+#pragma unroll
+            for (int j = 0; j < kDqChunks; ++j) {
+                if (j > 0) {
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    st_shared_v4(s_mine + sw128_offset(lane, u), __float_as_uint(scale * __uint_as_float(o[j][4 * u])),
+                                 __float_as_uint(scale * __uint_as_float(o[j][4 * u + 1])),
+                                 __float_as_uint(scale * __uint_as_float(o[j][4 * u + 2])),
+                                 __float_as_uint(scale * __uint_as_float(o[j][4 * u + 3])));
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && qrow < N) {
+                    tma_reduce_add_3d(&tm_dq, s_mine, hf * (D / 2) + 32 * j, qrow, bh);
+                    tma_store_commit();
+                }
+            }
         }
+        // Every reduction issued by this warp has completed (not only read).
+        if (lane == 0) tma_store_wait_all();
+        __syncwarp();
         // ------------------------------------------------------------ dK, dV
         // Warp-uniform: TMEM loads are collective; only the stores depend on
-        // the row.
-        const bool have = ok && n_q > 0 && wait_warp(bar(L::kBarDKV), 0, 28);
+        // the row.  Rows of hidden keys hold exact zeros.
+        const bool have = ok && n_q > 0 && wait_warp(bar(L::kBarDKV), 0, 30);
         if (have) tc_fence_after();
         if (ok) {
-            __nv_bfloat16 *pdv = dv + (static_cast<int64_t>(bh) * N + kj) * D;
-            __nv_bfloat16 *pdk = dk + (static_cast<int64_t>(bh) * N + kj) * D;
+            __nv_bfloat16 *pdv = dv + (static_cast<int64_t>(bh) * N + kj) * D + hf * (D / 2);
+            __nv_bfloat16 *pdk = dk + (static_cast<int64_t>(bh) * N + kj) * D + hf * (D / 2);
 #pragma unroll 1
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t a[32], g[32];
+            for (int c = 0; c < D / 64; ++c) {
+                uint32_t a[32], gk[32];
                 if (have) {
-                    tmem_ld32(t_lane + kTDV + 32 * c, a);
-                    tmem_ld32(t_lane + kTDV + D + 32 * c, g);
+                    tmem_ld32(t_lane + kTDV + hf * (D / 2) + 32 * c, a);
+                    tmem_ld32(t_lane + kTDV + D + hf * (D / 2) + 32 * c, gk);
                     tmem_ld_wait_only();
                     reg_fence(a);
-                    reg_fence(g);
+                    reg_fence(gk);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) a[e] = g[e] = 0u;
+                    for (int e = 0; e < 32; ++e) a[e] = gk[e] = 0u;
                 }
                 if (kj < N) {
 #pragma unroll
@@ -353,10 +417,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         wv.y = pack_bf16x2(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3]));
                         wv.z = pack_bf16x2(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5]));
                         wv.w = pack_bf16x2(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7]));
-                        wk.x = pack_bf16x2(scale * __uint_as_float(g[8 * u + 0]), scale * __uint_as_float(g[8 * u + 1]));
-                        wk.y = pack_bf16x2(scale * __uint_as_float(g[8 * u + 2]), scale * __uint_as_float(g[8 * u + 3]));
-                        wk.z = pack_bf16x2(scale * __uint_as_float(g[8 * u + 4]), scale * __uint_as_float(g[8 * u + 5]));
-                        wk.w = pack_bf16x2(scale * __uint_as_float(g[8 * u + 6]), scale * __uint_as_float(g[8 * u + 7]));
+                        wk.x = pack_bf16x2(scale * __uint_as_float(gk[8 * u + 0]), scale * __uint_as_float(gk[8 * u + 1]));
+                        wk.y = pack_bf16x2(scale * __uint_as_float(gk[8 * u + 2]), scale * __uint_as_float(gk[8 * u + 3]));
+                        wk.z = pack_bf16x2(scale * __uint_as_float(gk[8 * u + 4]), scale * __uint_as_float(gk[8 * u + 5]));
+                        wk.w = pack_bf16x2(scale * __uint_as_float(gk[8 * u + 6]), scale * __uint_as_float(gk[8 * u + 7]));
                         *reinterpret_cast<uint4 *>(pdv + 32 * c + 8 * u) = wv;
                         *reinterpret_cast<uint4 *>(pdk + 32 * c + 8 * u) = wk;
                     }
@@ -373,20 +437,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// D_i = dO_i . O_i (fp32) and dQ accumulator rows cleared; D/8 threads per row.
+// Per (head, padded query row): lse*log2e (+inf for a row with no visible key
+// or past N, so that exp2 gives P = 0), D_i = dO_i . O_i (0 past N), and the
+// row of the dQ accumulator cleared.  D/8 threads per row.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prepare(const __nv_bfloat16 *__restrict__ out,
-                                                   const __nv_bfloat16 *__restrict__ dout, float *__restrict__ dvec,
-                                                   float *__restrict__ dqacc, int64_t rows)
+                                                   const __nv_bfloat16 *__restrict__ dout,
+                                                   const float *__restrict__ lse, float *__restrict__ stats,
+                                                   float *__restrict__ dqacc, int N, int n_pad, int64_t rows_pad)
 {
     constexpr int kSeg = D / 8;
-    const int64_t row = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) / kSeg;
+    const int64_t prow = (static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x) / kSeg;
     const int seg = threadIdx.x % kSeg;
+    const int64_t bh = prow / n_pad;
+    const int q = static_cast<int>(prow - bh * n_pad);
+    const bool live = prow < rows_pad && q < N;
+    const int64_t row = bh * N + q;
     float acc = 0.f;
-    if (row < rows) {
+    if (live) {
         const uint4 o = *reinterpret_cast<const uint4 *>(out + row * D + seg * 8);
-        const uint4 g = *reinterpret_cast<const uint4 *>(dout + row * D + seg * 8);
-        const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {g.x, g.y, g.z, g.w};
+        const uint4 gv = *reinterpret_cast<const uint4 *>(dout + row * D + seg * 8);
+        const uint32_t ow[4] = {o.x, o.y, o.z, o.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             acc = fmaf(__uint_as_float(ow[i] << 16), __uint_as_float(gw[i] << 16), acc);
@@ -398,7 +469,15 @@ __global__ void __launch_bounds__(256) bwd_prepare(const __nv_bfloat16 *__restri
     }
 #pragma unroll
     for (int off = kSeg / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (row < rows && seg == 0) dvec[row] = acc;
+    if (prow < rows_pad && seg == 0) {
+        float l2 = INFINITY;
+        if (live) {
+            const float v = lse[row];
+            if (v > -INFINITY) l2 = v * kLog2e;
+        }
+        stats[prow] = l2;
+        stats[rows_pad + prow] = acc;
+    }
 }
 
 __global__ void __launch_bounds__(256) bwd_finish(const float *__restrict__ dqacc, __nv_bfloat16 *__restrict__ dq,
@@ -421,25 +500,26 @@ int launch_bwd(const BwdLaunch &a)
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (configured_device != dev) {
-        if (cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc) !=
+        if (cudaFuncSetAttribute(attn_bwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kBytes) !=
             cudaSuccess)
             return -1;
         configured_device = dev;
     }
-    const int64_t rows = static_cast<int64_t>(a.B) * a.H * a.N;
-    const int64_t seg_threads = rows * (D / 8);
-    bwd_prepare<D><<<static_cast<unsigned>((seg_threads + 255) / 256), 256, 0, a.stream>>>(
-        static_cast<const __nv_bfloat16 *>(a.out), static_cast<const __nv_bfloat16 *>(a.dout), a.dvec, a.dqacc,
-        rows);
-    if (cudaGetLastError() != cudaSuccess) return -1;
     const int n_tiles = (a.N + 127) / 128;
     const int num_bh = a.B * a.H;
-    attn_bwd_kernel<D><<<static_cast<unsigned>(n_tiles) * num_bh, kThreads, L::kAlloc, a.stream>>>(
-        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, a.lse, a.dvec, a.dqacc, static_cast<__nv_bfloat16 *>(a.dk),
-        static_cast<__nv_bfloat16 *>(a.dv), a.key_lens, a.H, a.N, n_tiles, num_bh, a.scale,
-        a.scale * kLog2e, a.causal);
+    const int n_pad = n_tiles * 128;
+    const int64_t rows_pad = static_cast<int64_t>(num_bh) * n_pad;
+    const int64_t seg_threads = rows_pad * (D / 8);
+    bwd_prepare<D><<<static_cast<unsigned>((seg_threads + 255) / 256), 256, 0, a.stream>>>(
+        static_cast<const __nv_bfloat16 *>(a.out), static_cast<const __nv_bfloat16 *>(a.dout), a.lse, a.stats,
+        a.dqacc, a.N, n_pad, rows_pad);
     if (cudaGetLastError() != cudaSuccess) return -1;
-    const int64_t n4 = rows * D / 4;
+    attn_bwd_kernel<D><<<static_cast<unsigned>(n_tiles) * num_bh, kThreads, L::kBytes, a.stream>>>(
+        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, a.stats, static_cast<__nv_bfloat16 *>(a.dk),
+        static_cast<__nv_bfloat16 *>(a.dv), a.key_lens, a.H, a.N, n_tiles, num_bh, a.scale, a.scale * kLog2e,
+        a.causal);
+    if (cudaGetLastError() != cudaSuccess) return -1;
+    const int64_t n4 = static_cast<int64_t>(num_bh) * a.N * D / 4;
     bwd_finish<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, a.stream>>>(a.dqacc,
                                                                             static_cast<__nv_bfloat16 *>(a.dq), n4);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;

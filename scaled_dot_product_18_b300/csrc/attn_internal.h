@@ -47,11 +47,12 @@ int attn_decode_launch(const DecodeLaunch &a);
 
 // Backward (dQ, dK, dV).
 struct BwdLaunch {
-    const CUtensorMap *tm_q, *tm_k, *tm_v, *tm_do;  // 4-D maps {d, N, H, B} bf16
+    const CUtensorMap *tm_q, *tm_k, *tm_v, *tm_do;  // 4-D maps {d, N, H, B} bf16, 64 x 128 boxes
+    const CUtensorMap *tm_dq;                       // 3-D map {d, N, B*H} fp32 over dqacc, 32 x 32 boxes
     const void *out, *dout;                         // bf16 [B*H*N, d] (contiguous)
     const float *lse;                               // [B*H*N] natural log, from the forward
-    float *dvec;                                    // [B*H*N] workspace: dO . O
-    float *dqacc;                                   // [B*H*N, d] workspace: fp32 dQ accumulator
+    float *stats;                                   // workspace [2][B*H][n_pad]: lse*log2e, D = dO . O
+    float *dqacc;                                   // workspace [B*H*N, d]: fp32 dQ accumulator
     void *dq, *dk, *dv;                             // bf16 [B*H*N, d]
     const int32_t *key_lens;
     int B, H, N, d;

@@ -174,9 +174,10 @@ def test_oracle_not_imported_by_product():
 
 
 def test_bwd_workspace_size(lib):
-    # fp32 dQ accumulator plus the fp32 D vector, each rounded up to 256 bytes
-    assert sdp.attn_bwd_workspace_size(2, 3, 5, 64) == 2 * 3 * 5 * 64 * 4 + 256
-    assert sdp.attn_bwd_workspace_size(1, 32, 16384, 128) == 32 * 16384 * (128 + 1) * 4
+    # fp32 dQ accumulator, then two fp32 values (lse*log2e, D) per query row
+    # padded to a multiple of 128; each part rounded up to 256 bytes
+    assert sdp.attn_bwd_workspace_size(2, 3, 5, 64) == 2 * 3 * 5 * 64 * 4 + 2 * 6 * 128 * 4
+    assert sdp.attn_bwd_workspace_size(1, 32, 16384, 128) == 32 * 16384 * (128 + 2) * 4
     assert sdp.attn_bwd_workspace_size(1, 1, 8, 96) == 0
     assert sdp.attn_bwd_workspace_size(0, 1, 8, 64) == 0
 
