@@ -12,25 +12,29 @@
 // that can see it (all of them, or those at or after the diagonal when
 // causal).  Per query tile, in tensor memory (512 columns):
 //   S^T = K Q_i^T          columns   0..127  (keys in TMEM lanes, queries in columns)
-//   dP^T = V dO_i^T        columns 128..255
-//   P^T -> bf16 packed over columns 0..31 and 64..95 of S^T (each half of
-//          the compute warps overwrites only columns it has read), the A
-//          operand of dV += P^T dO_i
-//   dS^T -> bf16 in shared memory (A operand of dK += dS^T Q_i, and, read
-//          query-major, of dQ_i = dS K, which lands in the dP^T columns)
+//   dP^T = V dO_i^T        columns 128..255, later dQ_i = dS K (queries in lanes)
+//   P^T -> bf16 packed over columns 0..31 and 64..95 of S^T, dS^T over
+//          columns 32..63 and 96..127 (each half of the compute warps
+//          overwrites only columns it has read): the TMEM A operands of
+//          dV += P^T dO_i and dK += dS^T Q_i
+//   dS^T -> also bf16 in shared memory, the A operand of the dQ MMA
 //   dV, dK accumulate in columns 256.. across the query tiles.
 // The MMA order per tile is S, dP, dV, dK, dQ: S^T is issued as soon as the
 // previous tile's dQ MMAs are queued, the compute warps turn S^T into P while
-// dP^T is being computed, and dS while dV is; dQ_i is added (times scale) to
-// an fp32 accumulator in global memory by TMA reductions staged through each
-// warp's own part of the dS^T buffer.  A pre-pass computes D, the scaled LSE
-// and clears the accumulator, a post-pass converts it to bf16.
+// dP^T is being computed, and dS while dV is.  Four dQ warps take dQ_i out of
+// tensor memory, stage it (times scale, fp32) in the (Q_i, dO_i) ring stage
+// that the tile's MMAs have finished with, and add it to an fp32 accumulator
+// in global memory with TMA reductions; they then hand the stage back to the
+// producer.  This keeps the accumulation off the compute warps' path.  A
+// pre-pass computes D and the scaled LSE and clears the accumulator; a
+// post-pass converts it to bf16.
 //
-//   warps 0-7  compute: warp w serves key rows 32 (w % 4) .. +31 (its TMEM
-//              lanes) and query columns 64 (w / 4) .. +63: P^T, dS^T; then
-//              dQ rows 32 (w % 4) .. of head-dim half w / 4; then dK and dV.
-//   warp 8     TMA producer: K, V once; (Q_i, dO_i, LSE, D) through a 2-stage ring.
-//   warp 9     allocates TMEM and issues the five MMAs of each query tile.
+//   warps 0-7   compute: warp w serves key rows 32 (w % 4) .. +31 (its TMEM
+//               lanes) and query columns 64 (w / 4) .. +63: P^T, dS^T; at
+//               the end dK and dV for head-dim half w / 4.
+//   warps 8-11  dQ: query rows 32 (w % 4) .. +31 of dQ_i.
+//   warp 12     TMA producer: K, V once; (Q_i, dO_i, LSE, D) through a 2-stage ring.
+//   warp 13     allocates TMEM and issues the five MMAs of each query tile.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -51,9 +55,10 @@ namespace {
 constexpr int kKeys = 128;    // keys per CTA
 constexpr int kQTile = 128;   // queries per step
 constexpr int kCompute = 8;   // compute warps
-constexpr int kThreads = (kCompute + 2) * 32;
-constexpr int kTmaWarp = kCompute;
-constexpr int kMmaWarp = kCompute + 1;
+constexpr int kDqWarp0 = kCompute;  // 4 dQ warps
+constexpr int kTmaWarp = kCompute + 4;
+constexpr int kMmaWarp = kCompute + 5;
+constexpr int kThreads = (kCompute + 6) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTS = 0, kTDP = 128, kTDV = 256;  // dK at kTDV + D
 constexpr float kLog2e = 1.4426950408889634f;
@@ -86,6 +91,8 @@ struct BwdSmem {
     static constexpr int kBytes = kOffMisc + 16;
     static_assert(kBytes <= 227 * 1024, "shared memory budget");
     static_assert(kTDV + 2 * D <= kTmemCols, "TMEM budget");
+    // dQ_i (128 x D fp32) is staged in one ring stage: 32 x 32 boxes of 4 KB.
+    static_assert(128 * D * 4 <= 2 * kTileBytes, "dQ staging fits a ring stage");
 };
 
 __device__ __forceinline__ uint32_t sw128_offset(int row, int chunk)
@@ -142,14 +149,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(bar(L::kBarKV), 1);
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(bar(L::kBarFull + s), 1);
-            mbar_init(bar(L::kBarEmpty + s), 1);
+            mbar_init(bar(L::kBarEmpty + s), 4 * 32);  // the dQ warps release a stage
         }
         mbar_init(bar(L::kBarS), 1);
         mbar_init(bar(L::kBarDP), 1);
         mbar_init(bar(L::kBarP), kCompute * 32);
         mbar_init(bar(L::kBarDS), kCompute * 32);
         mbar_init(bar(L::kBarDQ), 1);
-        mbar_init(bar(L::kBarDQUsed), kCompute * 32);
+        mbar_init(bar(L::kBarDQUsed), 4 * 32);
         mbar_init(bar(L::kBarDKV), 1);
         mbar_init(bar(L::kBarDrain), 1);
         *abort_flag = 0;
@@ -209,7 +216,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ok) break;
                 tc_fence_after();
                 // S^T = K Q_i^T (keys x queries, K = D).  The previous tile's P^T
-                // in these columns was consumed by its dV MMAs, queued earlier.
+                // and dS^T in these columns were consumed by its dV and dK MMAs,
+                // queued earlier.
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
@@ -239,10 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (ii > 0 || kk > 0) ? 1u : 0u);
                 if (!(ok = wait_warp(bar(L::kBarDS), ii & 1, 25))) break;
                 tc_fence_after();
-                // dK += dS^T Q_i: A = dS^T (keys x queries, K-major), B = Q_i query-major.
+                // dK += dS^T Q_i: A = dS^T from TMEM (packed next to P^T), B = Q_i query-major.
 #pragma unroll
                 for (int kk = 0; kk < kQTile / 16; ++kk)
-                    mma_bf16_ss_one(tm + kTDV + D, sdesc_sw128(sDS + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024),
+                    mma_bf16_ts_one(tm + kTDV + D, tm + kTS + 32 + (kk >> 2) * 64 + (kk & 3) * 8,
                                     sdesc_sw128(sQ(st) + kk * 16 * 128, 128 * 128, 1024), kIdKV,
                                     (ii > 0 || kk > 0) ? 1u : 0u);
                 // dQ_i = dS K: A = dS^T read query-major (M = queries), B = K key-major (N = D).
@@ -251,143 +259,146 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16_ss_one(tm + kTDP, sdesc_sw128(sDS + kk * 16 * 128, 128 * 128, 1024),
                                     sdesc_sw128(sK + kk * 16 * 128, 128 * 128, 1024), kIdQ, kk > 0 ? 1u : 0u);
                 mma_commit_one(bar(L::kBarDQ));
-                mma_commit_one(bar(L::kBarEmpty + st));
             }
             if (ok) mma_commit_one(bar(L::kBarDKV));
             mma_commit_one(bar(L::kBarDrain));
             wait_drain(bar(L::kBarDrain), 0);
         }
+    } else if (warp >= kDqWarp0) {
+        // ------------------------------------------------------------ dQ warps
+        const int g = warp & 3;  // TMEM lane quarter = query rows 32g..32g+31 of the tile
+        const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * g) << 16);
+        bool ok = true;
+        for (int ii = 0; ii < n_q && ok; ++ii) {
+            const int st = ii % L::kStages;
+            const int qrow = (i_first + ii) * kQTile + 32 * g;
+            if (!wait_warp(bar(L::kBarDQ), ii & 1, 26)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // The tile's dV and dK MMAs, which read this stage, finished before
+            // dQ_i did: stage this warp's 32 x D block there as D/32 boxes.
+            const uint32_t s_box = sQ(st) + g * (D / 32) * 4096;
+#pragma unroll 1
+            for (int j = 0; j < D / 32; ++j) {
+                uint32_t o[32];
+                tmem_ld32(t_lane + kTDP + 32 * j, o);
+                tmem_ld_wait(o);
+                if (j == D / 32 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(bar(L::kBarDQUsed));
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    st_shared_v4(s_box + j * 4096 + sw128_offset(lane, u),
+                                 __float_as_uint(scale * __uint_as_float(o[4 * u])),
+                                 __float_as_uint(scale * __uint_as_float(o[4 * u + 1])),
+                                 __float_as_uint(scale * __uint_as_float(o[4 * u + 2])),
+                                 __float_as_uint(scale * __uint_as_float(o[4 * u + 3])));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && qrow < N) {
+                for (int j = 0; j < D / 32; ++j) tma_reduce_add_3d(&tm_dq, s_box + j * 4096, 32 * j, qrow, bh);
+                tma_store_commit();
+            }
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            mbar_arrive(bar(L::kBarEmpty + st));
+        }
+        // Every reduction issued by this warp has completed (not only read).
+        if (lane == 0) tma_store_wait_all();
+        __syncwarp();
+        tc_fence_before();
     } else {
         // ------------------------------------------------------------ compute warps
-        const int g = warp & 3;   // TMEM lane quarter: key rows / dQ rows 32g..32g+31
-        const int hf = warp >> 2;  // query-column half (P, dS) and head-dim half (dQ, dK, dV)
+        const int g = warp & 3;   // TMEM lane quarter: key rows 32g..32g+31
+        const int hf = warp >> 2;  // query-column half (P, dS) and head-dim half (dK, dV)
         const int r = 32 * g + lane;  // key row == TMEM lane
         const int kj = k0 + r;
         const bool key_ok = kj < kv_len;
         const bool tail_keys = k0 + kKeys > kv_len;  // some key of this tile is hidden
         const uint32_t t_lane = tmem + (static_cast<uint32_t>(32 * g) << 16);
-        // This warp's 4 KB of the dS^T buffer (its key rows, its query half);
-        // between tiles it stages the warp's dQ boxes for the TMA reduction.
+        // This warp's 4 KB of the dS^T buffer (its key rows, its query half).
         const uint32_t s_mine = sDS + hf * (128 * 128) + g * 4096;
         bool ok = true;
         for (int ii = 0; ii < n_q && ok; ++ii) {
             const int st = ii % L::kStages;
             const int q0 = (i_first + ii) * kQTile;
             const bool masked = tail_keys || (causal && q0 == k0);  // per-element visibility needed
-            if (!wait_warp(bar(L::kBarFull + st), (ii / L::kStages) & 1, 26) || !wait_warp(bar(L::kBarS), ii & 1, 27)) {
+            // S_i done implies the previous tile's MMAs (dK, dQ reading dS^T) are done.
+            if (!wait_warp(bar(L::kBarFull + st), (ii / L::kStages) & 1, 27) || !wait_warp(bar(L::kBarS), ii & 1, 28)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             // P^T = exp2(S^T * scale*log2e - lse*log2e) over this warp's 64
-            // query columns, kept in fp32 for dS and stored as bf16 over the
-            // first 32 of those columns.
+            // query columns, 16 at a time; fp32 kept for dS, bf16 into TMEM.
             float p[64];
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c0 = 64 * hf + 32 * cc;  // first query column of the chunk
-                uint32_t sv[32];
-                tmem_ld32(t_lane + kTS + c0, sv);
-                float l2[32];
+            for (int c = 0; c < 4; ++c) {
+                const int c0 = 64 * hf + 16 * c;  // first query column of the step
+                uint32_t sv[16];
+                tmem_ld16(t_lane + kTS + c0, sv);
+                float l2[16];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
+                for (int e = 0; e < 4; ++e)
                     ld_shared_v4f(sStat(st) + (c0 + 4 * e) * 4, l2[4 * e], l2[4 * e + 1], l2[4 * e + 2], l2[4 * e + 3]);
                 tmem_ld_wait_only();
-                reg_fence(sv);
+                reg_fence16(sv);
                 if (!masked) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) p[32 * cc + e] = ex2(fmaf(__uint_as_float(sv[e]), scale_log2, -l2[e]));
+                    for (int e = 0; e < 16; ++e) p[16 * c + e] = ex2(fmaf(__uint_as_float(sv[e]), scale_log2, -l2[e]));
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
+                    for (int e = 0; e < 16; ++e) {
                         const bool vis = key_ok && (!causal || q0 + c0 + e >= kj);
-                        p[32 * cc + e] = vis ? ex2(fmaf(__uint_as_float(sv[e]), scale_log2, -l2[e])) : 0.f;
+                        p[16 * c + e] = vis ? ex2(fmaf(__uint_as_float(sv[e]), scale_log2, -l2[e])) : 0.f;
                     }
                 }
-                uint32_t pk[16];
+                uint32_t pk[8];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(p[32 * cc + 2 * e], p[32 * cc + 2 * e + 1]);
-                tmem_st16(t_lane + kTS + 64 * hf + 16 * cc, pk);
+                for (int e = 0; e < 8; ++e) pk[e] = pack_bf16x2(p[16 * c + 2 * e], p[16 * c + 2 * e + 1]);
+                tmem_st8(t_lane + kTS + 64 * hf + 8 * c, pk);
             }
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(L::kBarP));
-            // The warp's staging area held last tile's dQ boxes: wait until the
-            // TMA has read them before writing dS^T there.
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
-            if (!wait_warp(bar(L::kBarDP), ii & 1, 28)) {
+            if (!wait_warp(bar(L::kBarDP), ii & 1, 29)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // dS^T = P^T (dP^T - D) -> bf16, swizzled keys x queries in shared memory.
+            // dS^T = P^T (dP^T - D) -> bf16: into TMEM next to P^T and, swizzled
+            // keys x queries, into shared memory.
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
-                const int c0 = 64 * hf + 32 * cc;
-                uint32_t dpv[32];
-                tmem_ld32(t_lane + kTDP + c0, dpv);
-                float dd[32];
+            for (int c = 0; c < 4; ++c) {
+                const int c0 = 64 * hf + 16 * c;
+                uint32_t dpv[16];
+                tmem_ld16(t_lane + kTDP + c0, dpv);
+                float dd[16];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
+                for (int e = 0; e < 4; ++e)
                     ld_shared_v4f(sStat(st) + kQTile * 4 + (c0 + 4 * e) * 4, dd[4 * e], dd[4 * e + 1], dd[4 * e + 2],
                                   dd[4 * e + 3]);
                 tmem_ld_wait_only();
-                reg_fence(dpv);
-                uint32_t w[16];
+                reg_fence16(dpv);
+                uint32_t w[8];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack_bf16x2(p[32 * cc + 2 * e] * (__uint_as_float(dpv[2 * e]) - dd[2 * e]),
-                                       p[32 * cc + 2 * e + 1] * (__uint_as_float(dpv[2 * e + 1]) - dd[2 * e + 1]));
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int c16 = (c0 >> 3) + u - 8 * hf;  // 16-byte chunk within the half's 128-byte row
-                    st_shared_v4(s_mine + sw128_offset(lane, c16), w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-                }
+                for (int e = 0; e < 8; ++e)
+                    w[e] = pack_bf16x2(p[16 * c + 2 * e] * (__uint_as_float(dpv[2 * e]) - dd[2 * e]),
+                                       p[16 * c + 2 * e + 1] * (__uint_as_float(dpv[2 * e + 1]) - dd[2 * e + 1]));
+                tmem_st8(t_lane + kTS + 32 + 64 * hf + 8 * c, w);
+                const int c16 = 2 * c;  // 16-byte chunk within the half's 128-byte row
+                st_shared_v4(s_mine + sw128_offset(lane, c16), w[0], w[1], w[2], w[3]);
+                st_shared_v4(s_mine + sw128_offset(lane, c16 + 1), w[4], w[5], w[6], w[7]);
             }
+            tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(bar(L::kBarDS));
-            // dQ_i (queries in TMEM lanes): this warp's rows and head-dim half,
-            // times scale, added into the fp32 accumulator by TMA reductions.
-            if (!wait_warp(bar(L::kBarDQ), ii & 1, 29)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            constexpr int kDqChunks = D / 64;  // 32-column boxes per warp
-            uint32_t o[kDqChunks][32];
-#pragma unroll
-            for (int j = 0; j < kDqChunks; ++j) tmem_ld32(t_lane + kTDP + hf * (D / 2) + 32 * j, o[j]);
-            tmem_ld_wait_only();
-#pragma unroll
-            for (int j = 0; j < kDqChunks; ++j) reg_fence(o[j]);
-            tc_fence_before();
-            mbar_arrive(bar(L::kBarDQUsed));
-            const int qrow = q0 + 32 * g;
-#pragma unroll
-            for (int j = 0; j < kDqChunks; ++j) {
-                if (j > 0) {
-                    if (lane == 0) bulk_wait_read_all();
-                    __syncwarp();
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    st_shared_v4(s_mine + sw128_offset(lane, u), __float_as_uint(scale * __uint_as_float(o[j][4 * u])),
-                                 __float_as_uint(scale * __uint_as_float(o[j][4 * u + 1])),
-                                 __float_as_uint(scale * __uint_as_float(o[j][4 * u + 2])),
-                                 __float_as_uint(scale * __uint_as_float(o[j][4 * u + 3])));
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0 && qrow < N) {
-                    tma_reduce_add_3d(&tm_dq, s_mine, hf * (D / 2) + 32 * j, qrow, bh);
-                    tma_store_commit();
-                }
-            }
         }
-        // Every reduction issued by this warp has completed (not only read).
-        if (lane == 0) tma_store_wait_all();
-        __syncwarp();
         // ------------------------------------------------------------ dK, dV
         // Warp-uniform: TMEM loads are collective; only the stores depend on
         // the row.  Rows of hidden keys hold exact zeros.
