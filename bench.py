@@ -38,12 +38,21 @@ KERNEL_NAME = "attn_fwd_kernel"
 CSRC = os.path.join(ROOT, "scaled_dot_product_18_b300", "csrc")
 
 
-def kernel_source_sha() -> str:
+# Sources each timed kernel is compiled from (its own file plus the shared headers).
+KERNEL_SOURCES = {
+    "fwd": ("attn_fwd_sm103.cu", "ptx_sm103.cuh", "attn_internal.h"),
+    "bwd": ("attn_bwd_sm103.cu", "ptx_sm103.cuh", "attn_internal.h"),
+    "decode": ("attn_decode_sm103.cu", "ptx_sm103.cuh", "attn_internal.h"),
+}
+
+
+def kernel_source_sha(kind: str = "fwd") -> str:
+    """Hash of the sources of one kernel: a profile taken on another hash no
+    longer describes the code being timed."""
     h = hashlib.sha256()
-    for fn in sorted(os.listdir(CSRC)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            h.update(fn.encode())
-            h.update(open(os.path.join(CSRC, fn), "rb").read())
+    for fn in KERNEL_SOURCES[kind]:
+        h.update(fn.encode())
+        h.update(open(os.path.join(CSRC, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -343,7 +352,7 @@ def run_decode(args, w: I.DecodeWorkload, ws: int, rank: int, local: int) -> int
                 "ms_per_step": ms_e2e},
         "gpu_launches": 2 * args.steps,
         "clocks": sampler.summary(),
-        "kernel_src_sha": kernel_source_sha(),
+        "kernel_src_sha": kernel_source_sha("decode"),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -536,7 +545,7 @@ def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
                 "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in hout), "ms_per_step": ms_e2e},
         "gpu_launches": 3 * args.steps,
         "clocks": sampler.summary(),
-        "kernel_src_sha": kernel_source_sha(),
+        "kernel_src_sha": kernel_source_sha("bwd"),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
