@@ -65,7 +65,7 @@ def measured_peaks() -> dict:
     return {"bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "hbm_gbs": 6400.0, "source": "fallback"}
 
 
-def committed_traffic(workload: str):
+def committed_traffic(workload: str, kind: str = "fwd"):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
     on the current kernel source; otherwise None."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
@@ -74,7 +74,7 @@ def committed_traffic(workload: str):
     try:
         d = json.load(open(p))
         e = d.get(workload)
-        if e and e.get("kernel_src_sha") == kernel_source_sha():
+        if e and e.get("kernel_src_sha") == kernel_source_sha(kind):
             return float(e["dram_bytes_per_launch"])
     except (ValueError, KeyError):
         pass
@@ -537,7 +537,8 @@ def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
         "config": {"workload": w.name + "_backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "flops_per_step": flops, "l2": "inputs larger than L2"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                     "frac": achieved / peaks["bf16_tflops"],
+                     "traffic": committed_traffic(w.name + "_backward", "bwd"),
                      "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
                      "kernel": "attn_bwd_kernel (+ bwd_prepare, bwd_finish)"},
         "e2e": {"value": job_tflops(flops, ws, ms_e2e), "unit": "TFLOPS",
