@@ -196,7 +196,8 @@ def mha_block(x, w_qkv, w_o, H: int, causal: bool, key_lens=None, threads: int |
     return np.matmul(attn, w_o), lse
 
 
-def attention_backward_literal(q, k, v, dout, scale: float, causal: bool, key_lens=None, out=None):
+def attention_backward_literal(q, k, v, dout, scale: float, causal: bool, key_lens=None, out=None,
+                               window: int = 0):
     """Gradients of the attention forward with respect to Q, K and V, float64,
     from the materialised score matrix (tiny and moderate sizes):
 
@@ -212,9 +213,12 @@ def attention_backward_literal(q, k, v, dout, scale: float, causal: bool, key_le
     patterns).  When given, D_i is taken as dO_i . out_i -- the identity
     sum_j P_ij dP_ij = dO_i . (P V)_i applied to that stored output -- instead
     of from P and dP; everything else is unchanged.
+
+    window: the sliding window of attention_literal (query i sees keys
+    j > i - window when > 0); P, and so every gradient, follows it.
     """
     q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
-    _, _, P = attention_literal(q, k, v, scale, causal, key_lens)
+    _, _, P = attention_literal(q, k, v, scale, causal, key_lens, window)
     dV = np.matmul(np.swapaxes(P, -1, -2), dout)
     dP = np.matmul(dout, np.swapaxes(v, -1, -2))
     if out is None:

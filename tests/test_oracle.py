@@ -459,8 +459,8 @@ def test_mha_block_head_permutation_invariance():
 
 # --- backward: gradients of the forward ------------------------------------------
 
-def _loss(q, k, v, g, scale, causal, kl):
-    O, _, _ = oracle.attention_literal(q, k, v, scale, causal, kl)
+def _loss(q, k, v, g, scale, causal, kl, window=0):
+    O, _, _ = oracle.attention_literal(q, k, v, scale, causal, kl, window)
     return float((O * g).sum())
 
 
@@ -485,6 +485,39 @@ def test_backward_matches_finite_differences(causal):
             num[idx] = (up - dn) / (2 * eps)
         np.testing.assert_allclose(dX, num, atol=1e-7)
     assert np.all(dK[:, :, 4:] == 0.0) and np.all(dV[:, :, 4:] == 0.0)  # hidden keys get no gradient
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_window_matches_finite_differences(causal):
+    # The sliding window (query i sees keys j > i - w) changes which scores
+    # exist; the gradients must be those of that function.
+    r = np.random.default_rng(65)
+    B, H, N, d, w = 1, 1, 7, 3, 3
+    q, k, v, g = (r.standard_normal((B, H, N, d)) for _ in range(4))
+    kl = np.array([6], dtype=np.int32)
+    dQ, dK, dV = oracle.attention_backward_literal(q, k, v, g, 0.6, causal, kl, window=w)
+    eps = 1e-6
+    for X, dX in ((q, dQ), (k, dK), (v, dV)):
+        num = np.zeros_like(X)
+        for idx in np.ndindex(X.shape):
+            old = X[idx]
+            X[idx] = old + eps
+            up = _loss(q, k, v, g, 0.6, causal, kl, w)
+            X[idx] = old - eps
+            dn = _loss(q, k, v, g, 0.6, causal, kl, w)
+            X[idx] = old
+            num[idx] = (up - dn) / (2 * eps)
+        np.testing.assert_allclose(dX, num, atol=1e-7)
+    # with causal and w = 1 every row sees only itself: P = I, so dV = dO and
+    # dS = P (dP - D) = 0 gives dQ = dK = 0 (on the rows whose key is visible)
+    dQ1, dK1, dV1 = oracle.attention_backward_literal(q, k, v, g, 0.6, True, None, window=1)
+    np.testing.assert_allclose(dV1, g, atol=1e-12)
+    np.testing.assert_allclose(dQ1, 0.0, atol=1e-12)
+    np.testing.assert_allclose(dK1, 0.0, atol=1e-12)
+    # a window covering everything is no window
+    for a, b_ in zip(oracle.attention_backward_literal(q, k, v, g, 0.6, causal, kl, window=N),
+                     oracle.attention_backward_literal(q, k, v, g, 0.6, causal, kl)):
+        np.testing.assert_array_equal(a, b_)
 
 
 def test_backward_sampled_matches_literal():
