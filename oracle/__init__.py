@@ -232,13 +232,14 @@ def attention_backward_literal(q, k, v, dout, scale: float, causal: bool, key_le
 
 
 def attention_backward_sampled(q, k, v, dout, scale: float, causal: bool, key_lens=None, heads=None,
-                               q_rows=None, k_rows=None, out=None):
+                               q_rows=None, k_rows=None, out=None, window: int = 0):
     """The same gradients for selected (b, h) heads, dQ rows and dK/dV rows,
     without the full N x N matrix: each row of P is rebuilt from the row
     oracle's log-sum-exp, P_ij = exp(s_ij - lse_i) over the visible keys.
     out: optional stored forward output [B, H, N, d]; D_i is then dO_i . out_i
-    (as in attention_backward_literal).  Returns dicts keyed by (b, h): dQ
-    [len(q_rows), d], dK and dV [len(k_rows), d]."""
+    (as in attention_backward_literal).  window: the forward's sliding window
+    (query i sees keys j > i - window when > 0).  Returns dicts keyed by
+    (b, h): dQ [len(q_rows), d], dK and dV [len(k_rows), d]."""
     q, k, v, dout = _as_f64(q), _as_f64(k), _as_f64(v), _as_f64(dout)
     stored = out
     B, H, N, d = q.shape
@@ -246,7 +247,7 @@ def attention_backward_sampled(q, k, v, dout, scale: float, causal: bool, key_le
     for b, h in heads:
         kl = N if key_lens is None else int(key_lens[b])
         O, lse = attention_rows(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], scale, causal,
-                                None if key_lens is None else np.array([kl], dtype=np.int32))
+                                None if key_lens is None else np.array([kl], dtype=np.int32), window=window)
         O, lse = O[0, 0], lse[0, 0]
         if stored is not None:
             O = _as_f64(stored[b, h])
@@ -257,6 +258,8 @@ def attention_backward_sampled(q, k, v, dout, scale: float, causal: bool, key_le
             keep = np.arange(N) < kl
             if causal:
                 keep &= np.arange(N) <= i
+            if window > 0:
+                keep &= np.arange(N) > i - window
             if not np.isfinite(lse[i]):
                 return np.zeros(N)
             s = scale * (kb @ qb[i])
@@ -272,7 +275,7 @@ def attention_backward_sampled(q, k, v, dout, scale: float, causal: bool, key_le
         for r, j in enumerate(k_rows):
             col = np.zeros(N)  # P[:, j]
             for i in range(N):
-                if j < kl and (not causal or j <= i) and np.isfinite(lse[i]):
+                if j < kl and (not causal or j <= i) and (window <= 0 or j > i - window) and np.isfinite(lse[i]):
                     col[i] = np.exp(scale * (qb[i] @ kb[j]) - lse[i])
             dpj = db @ vb[j]  # dP[:, j]
             ds = col * (dpj - Dvec)

@@ -534,6 +534,14 @@ def test_backward_sampled_matches_literal():
             np.testing.assert_allclose(sq, dQ[b, h, rows], atol=1e-11)
             np.testing.assert_allclose(sk, dK[b, h, rows], atol=1e-11)
             np.testing.assert_allclose(sv, dV[b, h, rows], atol=1e-11)
+        # and with a sliding window
+        dQ, dK, dV = oracle.attention_backward_literal(q, k, v, g, 0.4, causal, kl, window=9)
+        got = oracle.attention_backward_sampled(q, k, v, g, 0.4, causal, kl, heads=[(0, 1), (1, 0)], q_rows=rows,
+                                                k_rows=rows, window=9)
+        for (b, h), (sq, sk, sv) in got.items():
+            np.testing.assert_allclose(sq, dQ[b, h, rows], atol=1e-11)
+            np.testing.assert_allclose(sk, dK[b, h, rows], atol=1e-11)
+            np.testing.assert_allclose(sv, dV[b, h, rows], atol=1e-11)
 
 
 def test_backward_with_stored_output_identity():
