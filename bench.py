@@ -456,7 +456,8 @@ def run_mha(args, w: I.MhaWorkload, ws: int, rank: int, local: int) -> int:
 def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
     """The backward (dQ, dK, dV) of one workload: TFLOPS over the nominal
     backward flops, 2.5x the forward's (five N x N x d contractions per head
-    instead of two: S, dP, dV, dK, dQ), halved when causal."""
+    instead of two: S, dP, dV, dK, dQ), halved when causal; with --window the
+    forward's count is that of the visible (query, key) pairs."""
     import torch
     import torch.distributed as dist
 
@@ -470,7 +471,7 @@ def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
     dev = lambda b: torch.from_numpy(b.view(np.int16)).cuda().view(torch.bfloat16)  # noqa: E731
     q, k, v, do = dev(x.q), dev(x.k), dev(x.v), dev(hdo)
     kl = torch.from_numpy(x.key_lens).cuda() if x.key_lens is not None else None
-    out, lse = sdp.attention(q, k, v, causal=w.causal, key_lens=kl, scale=w.scale)
+    out, lse = sdp.attention(q, k, v, causal=w.causal, key_lens=kl, scale=w.scale, window=args.window)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     nbytes = sdp.attn_bwd_workspace_size(w.B, w.H, w.N, w.d)
     wsbuf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
@@ -478,8 +479,12 @@ def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
     sh = stream.cuda_stream
 
     def step():
-        st = sdp.attn_bwd(q, k, v, out, do, lse, dq, dk, dv, w.B, w.H, w.N, w.d, w.scale, w.causal, kl, wsbuf,
-                          nbytes, sh)
+        if args.window:
+            st = sdp.attn_bwd_window(q, k, v, out, do, lse, dq, dk, dv, w.B, w.H, w.N, w.d, w.scale, w.causal, kl,
+                                     args.window, wsbuf, nbytes, sh)
+        else:
+            st = sdp.attn_bwd(q, k, v, out, do, lse, dq, dk, dv, w.B, w.H, w.N, w.d, w.scale, w.causal, kl, wsbuf,
+                              nbytes, sh)
         if st != sdp.ATTN_OK:
             raise sdp.AttnError(st, "attn_bwd")
 
@@ -528,7 +533,7 @@ def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(e2.elapsed_time(e3) / args.e2e_steps, ws, "cuda")
     peaks = measured_peaks()
-    flops = 2.5 * w.flops()
+    flops = 2.5 * (window_flops(w, args.window) if args.window else w.flops())
     achieved = flops / (ms_step * 1e-3) / 1e12
     line = {
         "metric": "attention_bwd_tflops", "value": job_tflops(flops, ws, ms_step), "unit": "TFLOPS", "n_gpus": ws,

@@ -239,7 +239,21 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *ou
                      const int32_t *key_lens, void *workspace, size_t workspace_bytes,
                      attn_stream_t stream);
 
-/* Bytes of workspace attn_bwd needs (0 for invalid sizes). */
+/*
+ * attn_bwd_window -- attn_bwd for the forward of attn_fwd_window: the same
+ * arguments, layout, ownership and errors, plus
+ * window  : >= 0, the forward's window (query i sees keys j > i - window when
+ *           0 < window < N; 0 or >= N: none).  Negative -> ATTN_EINVAL.  lse
+ *           and out must come from attn_fwd_window with the same window.  Key
+ *           tiles meet only the query tiles inside their windows.
+ */
+attn_status attn_bwd_window(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                            const float *lse, void *dq, void *dk, void *dv,
+                            int B, int H, int N, int d, float scale, int causal,
+                            const int32_t *key_lens, int window, void *workspace, size_t workspace_bytes,
+                            attn_stream_t stream);
+
+/* Bytes of workspace attn_bwd and attn_bwd_window need (0 for invalid sizes). */
 size_t attn_bwd_workspace_size(int B, int H, int N, int d);
 
 /*
@@ -256,7 +270,7 @@ const char *attn_status_str(attn_status s);
 /* ABI version of this header (bumped on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 4
+#define ATTN_ABI_VERSION 5
 
 #ifdef __cplusplus
 }

@@ -28,7 +28,7 @@ ATTN_ETOOLARGE = -6
 
 # Symbols declared in include/attn.h.
 EXPORTS = ("attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_workspace_size", "attn_decode_noalloc",
-           "attn_mha_fwd", "attn_mha_workspace_size", "attn_bwd", "attn_bwd_workspace_size", "attn_check_device",
+           "attn_mha_fwd", "attn_mha_workspace_size", "attn_bwd", "attn_bwd_window", "attn_bwd_workspace_size", "attn_check_device",
            "attn_status_str", "attn_abi_version")
 
 _lib = None
@@ -66,6 +66,9 @@ def load_library():
     lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, vp, vp,
                              ctypes.c_size_t, vp]
     lib.attn_bwd.restype = i
+    lib.attn_bwd_window.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, vp, i, vp,
+                                    ctypes.c_size_t, vp]
+    lib.attn_bwd_window.restype = i
     lib.attn_bwd_workspace_size.argtypes = [i, i, i, i]
     lib.attn_bwd_workspace_size.restype = ctypes.c_size_t
     lib.attn_check_device.argtypes = [vp]
@@ -178,15 +181,25 @@ def attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, B: int, H: int, N: int, d: int
                         _ptr(workspace), int(workspace_bytes), _stream(stream))
 
 
+def attn_bwd_window(q, k, v, out, dout, lse, dq, dk, dv, B: int, H: int, N: int, d: int, scale: float, causal,
+                    key_lens=None, window: int = 0, workspace=None, workspace_bytes: int = 0, stream=None) -> int:
+    """The C ``attn_bwd_window``: the backward of the sliding-window forward."""
+    lib = load_library()
+    return lib.attn_bwd_window(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                               _ptr(dv), int(B), int(H), int(N), int(d), float(scale), 1 if causal else 0,
+                               _ptr(key_lens), int(window), _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
 def attn_bwd_workspace_size(B: int, H: int, N: int, d: int) -> int:
     return int(load_library().attn_bwd_workspace_size(int(B), int(H), int(N), int(d)))
 
 
 def attention_backward(q, k, v, out, lse, dout, causal: bool = False, key_lens=None, scale: float | None = None,
-                       stream=None, workspace=None):
-    """Convenience wrapper over ``attn_bwd`` for torch tensors of the forward's
-    layout; allocates dq, dk, dv (and the workspace when not given) with torch
-    and raises ``AttnError`` on a non-OK status.  Returns (dq, dk, dv)."""
+                       stream=None, workspace=None, window: int = 0):
+    """Convenience wrapper over ``attn_bwd`` (``attn_bwd_window`` when window >
+    0) for torch tensors of the forward's layout; allocates dq, dk, dv (and the
+    workspace when not given) with torch and raises ``AttnError`` on a non-OK
+    status.  Returns (dq, dk, dv)."""
     import torch
     B, H, N, d = q.shape
     for t in (q, k, v, out, dout):
@@ -200,8 +213,13 @@ def attention_backward(q, k, v, out, lse, dout, causal: bool = False, key_lens=N
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    st = attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, key_lens, workspace,
-                  workspace.numel() * workspace.element_size(), stream)
+    nbytes = workspace.numel() * workspace.element_size()
+    if window:
+        st = attn_bwd_window(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, key_lens, window,
+                             workspace, nbytes, stream)
+    else:
+        st = attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, key_lens, workspace, nbytes,
+                      stream)
     if st != ATTN_OK:
         raise AttnError(st, "attn_bwd")
     return dq, dk, dv

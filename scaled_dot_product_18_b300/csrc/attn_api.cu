@@ -314,11 +314,14 @@ bool make_dq_map(CUtensorMap *m, float *base, int64_t BH, int N, int d)
 
 }  // namespace
 
-attn_status attn_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
+namespace {
+
+attn_status backward(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
                      void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal,
-                     const int32_t *key_lens, void *workspace, size_t workspace_bytes, attn_stream_t stream)
+                     const int32_t *key_lens, int window, void *workspace, size_t workspace_bytes,
+                     attn_stream_t stream)
 {
-    if (B < 0 || H < 0 || N < 0) return ATTN_EINVAL;
+    if (B < 0 || H < 0 || N < 0 || window < 0) return ATTN_EINVAL;
     if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
     if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_EINVAL;
     if (B == 0 || H == 0 || N == 0) return ATTN_OK;
@@ -363,10 +366,30 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *ou
     a.d = d;
     a.scale = scale;
     a.causal = causal ? 1 : 0;
+    a.window = window >= N ? 0 : window;
     a.stream = reinterpret_cast<cudaStream_t>(stream);
     const int rc = sdp18::attn_bwd_launch(a);
     if (rc == -2) return ATTN_EUNSUPPORTED;
     return rc == 0 ? ATTN_OK : ATTN_ECUDA;
+}
+
+}  // namespace
+
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout, const float *lse,
+                     void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale, int causal,
+                     const int32_t *key_lens, void *workspace, size_t workspace_bytes, attn_stream_t stream)
+{
+    return backward(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, key_lens, 0, workspace,
+                    workspace_bytes, stream);
+}
+
+attn_status attn_bwd_window(const void *q, const void *k, const void *v, const void *out, const void *dout,
+                            const float *lse, void *dq, void *dk, void *dv, int B, int H, int N, int d, float scale,
+                            int causal, const int32_t *key_lens, int window, void *workspace, size_t workspace_bytes,
+                            attn_stream_t stream)
+{
+    return backward(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, scale, causal, key_lens, window, workspace,
+                    workspace_bytes, stream);
 }
 
 attn_status attn_check_device(attn_stream_t stream)

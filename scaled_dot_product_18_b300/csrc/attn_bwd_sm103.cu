@@ -10,7 +10,8 @@
 //
 // One CTA owns a 128-key tile of one (batch, head) and walks the query tiles
 // that can see it (all of them, or those at or after the diagonal when
-// causal).  Per query tile, in tensor memory (512 columns):
+// causal, and with a sliding window of w positions -- query i sees keys
+// j > i - w -- only those before query k0 + 127 + w).  Per query tile, in tensor memory (512 columns):
 //   S^T = K Q_i^T          columns   0..127  (keys in TMEM lanes, queries in columns)
 //   dP^T = V dO_i^T        columns 128..255, later dQ_i = dS K (queries in lanes)
 //   P^T -> bf16 packed over columns 0..31 and 64..95 of S^T, dS^T over
@@ -112,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_dq, const float *__restrict__ stats,
                     __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
                     const int32_t *__restrict__ key_lens, int H, int N, int n_tiles, int num_bh, float scale,
-                    float scale_log2, int causal)
+                    float scale_log2, int causal, int window)
 {
     using L = BwdSmem<D>;
     // The tiles are 128-byte swizzled and need a 1024-byte aligned base.  The
@@ -141,8 +142,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int kv_len = N;
     if (key_lens != nullptr) kv_len = min(max(key_lens[b], 0), N);
     const int k0 = kt * kKeys;
+    // Query tiles this key tile meets: from the diagonal when causal, up to
+    // the last query whose window reaches the tile's last visible key.
     const int i_first = (causal && k0 < kv_len) ? kt : 0;
-    const int n_q = k0 < kv_len ? n_tiles - i_first : 0;  // query tiles this key tile meets
+    int i_last = n_tiles - 1;
+    if (window > 0 && k0 < kv_len) {
+        const int64_t i_max = static_cast<int64_t>(min(k0 + kKeys, kv_len) - 1) + window - 1;
+        i_last = static_cast<int>(i_max / kQTile < i_last ? i_max / kQTile : i_last);
+    }
+    const int n_q = k0 < kv_len ? max(0, i_last - i_first + 1) : 0;
     const int n_pad = n_tiles * kQTile;
 
     if (threadIdx.x == 0) {
@@ -326,7 +334,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ii = 0; ii < n_q && ok; ++ii) {
             const int st = ii % L::kStages;
             const int q0 = (i_first + ii) * kQTile;
-            const bool masked = tail_keys || (causal && q0 == k0);  // per-element visibility needed
+            // per-element visibility needed: hidden keys, the diagonal, or
+            // queries past some key's window (i >= j + w) in this tile
+            const bool masked = tail_keys || (causal && q0 == k0) || (window > 0 && q0 + kQTile - 1 - k0 >= window);
             // S_i done implies the previous tile's MMAs (dK, dQ reading dS^T) are done.
             if (!wait_warp(bar(L::kBarFull + st), (ii / L::kStages) & 1, 27) || !wait_warp(bar(L::kBarS), ii & 1, 28)) {
                 ok = false;
@@ -353,7 +363,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
-                        const bool vis = key_ok && (!causal || q0 + c0 + e >= kj);
+                        const int qi = q0 + c0 + e;
+                        const bool vis = key_ok && (!causal || qi >= kj) && (window <= 0 || qi - kj < window);
                         p[16 * c + e] = vis ? ex2(fmaf(__uint_as_float(sv[e]), scale_log2, -l2[e])) : 0.f;
                     }
                 }
@@ -528,7 +539,7 @@ int launch_bwd(const BwdLaunch &a)
     attn_bwd_kernel<D><<<static_cast<unsigned>(n_tiles) * num_bh, kThreads, L::kBytes, a.stream>>>(
         *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, a.stats, static_cast<__nv_bfloat16 *>(a.dk),
         static_cast<__nv_bfloat16 *>(a.dv), a.key_lens, a.H, a.N, n_tiles, num_bh, a.scale, a.scale * kLog2e,
-        a.causal);
+        a.causal, a.window);
     if (cudaGetLastError() != cudaSuccess) return -1;
     const int64_t n4 = static_cast<int64_t>(num_bh) * a.N * D / 4;
     bwd_finish<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, a.stream>>>(a.dqacc,

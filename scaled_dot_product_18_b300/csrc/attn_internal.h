@@ -58,6 +58,7 @@ struct BwdLaunch {
     int B, H, N, d;
     float scale;
     int causal;
+    int window;  // > 0: query i sees keys j > i - window
     cudaStream_t stream;
 };
 // 0 on success, -1 on a CUDA error, -2 for an unsupported head dimension.

@@ -30,7 +30,8 @@ def declared_functions():
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert {"attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_workspace_size", "attn_mha_fwd",
-            "attn_mha_workspace_size", "attn_bwd", "attn_bwd_workspace_size", "attn_check_device", "attn_status_str",
+            "attn_mha_workspace_size", "attn_bwd", "attn_bwd_window", "attn_bwd_workspace_size", "attn_check_device",
+            "attn_status_str",
             "attn_abi_version"} <= names
     assert names == set(sdp.EXPORTS)
     for n in names:
@@ -38,7 +39,7 @@ def test_exports_every_declared_symbol(lib):
 
 
 def test_abi_version_and_status_strings(lib):
-    assert sdp.attn_abi_version() == 4
+    assert sdp.attn_abi_version() == 5
     for code in (0, -1, -2, -3, -4, -5):
         assert sdp.attn_status_str(code).startswith("ATTN_")
     assert sdp.attn_status_str(7) == "unknown attn_status"
@@ -214,3 +215,19 @@ def test_bwd_host_side_rejections(lib, args, want):
                       a["H"], a["N"], a["d"], a["scale"], a["causal"], a["key_lens"], a["ws"], a["ws_bytes"],
                       a["stream"])
     assert st == want, (args, st)
+
+
+@pytest.mark.parametrize("window,want", [(-1, sdp.ATTN_EINVAL), (-7, sdp.ATTN_EINVAL)])
+def test_bwd_window_rejections(lib, window, want):
+    st = lib.attn_bwd_window(P, P, P, P, P, P, P, P, P, 2, 3, 5, 64, 0.125, 1, None, window, P, 1 << 30, None)
+    assert st == want
+
+
+def test_bwd_window_host_checks_match_attn_bwd(lib):
+    # same argument checks as attn_bwd (window 0 = none)
+    assert lib.attn_bwd_window(P, P, P, P, P, P, P, P, P, 2, 3, 5, 96, 0.125, 1, None, 4, P, 1 << 30,
+                               None) == sdp.ATTN_EUNSUPPORTED
+    assert lib.attn_bwd_window(P, P, P, P, P, None, P, P, P, 2, 3, 5, 64, 0.125, 1, None, 4, P, 1 << 30,
+                               None) == sdp.ATTN_EINVAL
+    assert lib.attn_bwd_window(None, None, None, None, None, None, None, None, None, 0, 3, 5, 64, 0.125, 1, None, 4,
+                               None, 0, None) == sdp.ATTN_OK

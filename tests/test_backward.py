@@ -36,7 +36,7 @@ ABS_FLOOR = 1e-4
 GUARD = 4096
 
 
-def run_bwd(q, k, v, dout, scale, causal, key_lens=None, want_out=False):
+def run_bwd(q, k, v, dout, scale, causal, key_lens=None, want_out=False, window=0):
     """Forward then backward through the C ABI; gradients as float64 arrays
     (and the forward's bf16 output, as float64, with want_out).  dq/dk/dv
     live inside NaN-filled buffers whose tails must stay NaN."""
@@ -44,13 +44,17 @@ def run_bwd(q, k, v, dout, scale, causal, key_lens=None, want_out=False):
     B, H, N, d = q.shape
     tq, tk, tv, tdo = (to_dev(x) for x in (q, k, v, dout))
     kl = t.from_numpy(np.asarray(key_lens, dtype=np.int32)).cuda() if key_lens is not None else None
-    out, lse = sdp.attention(tq, tk, tv, causal=causal, key_lens=kl, scale=scale)
+    out, lse = sdp.attention(tq, tk, tv, causal=causal, key_lens=kl, scale=scale, window=window)
     n = B * H * N * d
     bufs = [t.full((n + GUARD,), float("nan"), dtype=t.bfloat16, device="cuda") for _ in range(3)]
     ws = t.full((sdp.attn_bwd_workspace_size(B, H, N, d),), 0xFF, dtype=t.uint8, device="cuda")
     stream = t.cuda.current_stream()
-    st = sdp.attn_bwd(tq, tk, tv, out, tdo, lse, bufs[0], bufs[1], bufs[2], B, H, N, d, scale, causal, kl, ws,
-                      ws.numel(), stream)
+    if window:
+        st = sdp.attn_bwd_window(tq, tk, tv, out, tdo, lse, bufs[0], bufs[1], bufs[2], B, H, N, d, scale, causal, kl,
+                                 window, ws, ws.numel(), stream)
+    else:
+        st = sdp.attn_bwd(tq, tk, tv, out, tdo, lse, bufs[0], bufs[1], bufs[2], B, H, N, d, scale, causal, kl, ws,
+                          ws.numel(), stream)
     assert st == sdp.ATTN_OK, sdp.attn_status_str(st)
     assert sdp.attn_check_device(stream) == sdp.ATTN_OK
     res = []
@@ -159,5 +163,57 @@ def test_backward_sampled_full_size(name):
     for (b, h) in heads:
         mine = [g[b, h, rows] for g in got]
         check_grads(mine, None, ref[(b, h)], ref_stored[(b, h)], "%s b%d h%d" % (name, b, h))
+    for G in got:
+        assert np.isfinite(G).all()
+
+
+WINDOW_CASES = [(1, 129, 1), (2, 300, 64), (2, 300, 127), (2, 300, 129), (1, 700, 200), (2, 257, 300)]
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_window_grid(d, causal):
+    # attn_bwd_window against the oracle's windowed backward (query i sees
+    # keys j > i - w), with key lengths on two-batch cases; w >= N is no window.
+    for B, N, w in WINDOW_CASES:
+        H = 2
+        seed = 17 * N + w + d + (7 if causal else 0)
+        q, k, v, do = (I.make_tensor_bits(seed, s, (B, H, N, d)) for s in (0, 1, 2, 4))
+        kla = np.array([max(1, (2 * N) // 3), N][:B], dtype=np.int32) if B == 2 else None
+        scale = 1.0 / np.sqrt(d)
+        got, O = run_bwd(q, k, v, do, scale, causal, kla, want_out=True, window=w)
+        ref = oracle.attention_backward_literal(q, k, v, do, scale, causal, kla, window=w)
+        ref_stored = oracle.attention_backward_literal(q, k, v, do, scale, causal, kla, out=O, window=w)
+        check_grads(got, O, ref, ref_stored, "window N%d w%d d%d causal=%s kl=%s" % (N, w, d, causal, kla))
+
+
+def test_backward_window_covering_everything_matches_attn_bwd():
+    B, H, N, d = 2, 2, 333, 128
+    q, k, v, do = (I.make_tensor_bits(91, s, (B, H, N, d)) for s in (0, 1, 2, 4))
+    kl = np.array([200, 333], dtype=np.int32)
+    for causal in (False, True):
+        a = run_bwd(q, k, v, do, 0.09, causal, kl)
+        b = run_bwd(q, k, v, do, 0.09, causal, kl, window=N + 5)
+        np.testing.assert_array_equal(a[1], b[1])
+        np.testing.assert_array_equal(a[2], b[2])
+
+
+def test_backward_window_sampled_full_size():
+    # The long-context workload with the pages' window of 512 (the launch
+    # `bench.py --backward --window 512` times); sampled rows of two heads.
+    w = I.WORKLOADS["c5_b1h32n16384d128_causal"]
+    window = 512
+    x = I.make_inputs(w)
+    do = I.make_dout(w)
+    got, O = run_bwd(x.q, x.k, x.v, do, w.scale, w.causal, x.key_lens, want_out=True, window=window)
+    rng = np.random.default_rng(7)
+    heads = [(0, 0), (0, w.H - 1)]
+    rows = _sample(w.N, rng)
+    kw = dict(heads=heads, q_rows=rows, k_rows=rows, window=window)
+    ref = oracle.attention_backward_sampled(x.q, x.k, x.v, do, w.scale, w.causal, x.key_lens, **kw)
+    ref_stored = oracle.attention_backward_sampled(x.q, x.k, x.v, do, w.scale, w.causal, x.key_lens, out=O, **kw)
+    for (b, h) in heads:
+        mine = [g[b, h, rows] for g in got]
+        check_grads(mine, None, ref[(b, h)], ref_stored[(b, h)], "window512 b%d h%d" % (b, h))
     for G in got:
         assert np.isfinite(G).all()
