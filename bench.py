@@ -510,27 +510,74 @@ def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
     ms_step = max_over_ranks(e0.elapsed_time(e1), ws, "cuda") / args.steps
     if sdp.attn_check_device(sh) != sdp.ATTN_OK:
         raise RuntimeError("device error in timed steps")
-    # end to end: q, k, v, O, dO and lse go up, dQ, dK, dV come back
-    pin = lambda t: t.cpu().pin_memory()  # noqa: E731
-    hin = [pin(t) for t in (q, k, v, out, do, lse)]
-    hout = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    # end to end: q, k, v, O, dO and lse go up, dq, dk, dv come back.  As in
+    # the forward, the step is pipelined over chunks of whole batches (B > 1)
+    # or groups of heads (B == 1) on three streams; each chunk is one attn_bwd
+    # call on contiguous slices (the workspace is reused in stream order).
+    dev_in = (q, k, v, out, do, lse)
+    dev_out = (dq, dk, dv)
+    ref_dk, ref_dv = dk.clone(), dv.clone()
+    hin = [t_.cpu().pin_memory() for t_ in dev_in]
+    hout = [torch.empty(t_.shape, dtype=t_.dtype).pin_memory() for t_ in dev_out]
+    if w.B > 1:
+        n_chunks = min(w.B, 8)
+        bounds = [(w.B * i // n_chunks, w.B * (i + 1) // n_chunks) for i in range(n_chunks)]
+        per = w.H * w.N
+    else:
+        n_chunks = min(w.H, 8)
+        bounds = [(w.H * i // n_chunks, w.H * (i + 1) // n_chunks) for i in range(n_chunks)]
+        per = w.N
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in bounds]
+    ev_done = [torch.cuda.Event() for _ in bounds]
+    ev_out = [torch.cuda.Event() for _ in bounds]
+    rows = lambda t_: t_.view(-1, w.d) if t_.dim() == 4 else t_.view(-1)  # noqa: E731
+    din, dout_ = [rows(t_) for t_ in dev_in], [rows(t_) for t_ in dev_out]
+    hinf, houtf = [rows(t_) for t_ in hin], [rows(t_) for t_ in hout]
 
     def e2e_step():
-        for d_, h_ in zip((q, k, v, out, do, lse), hin):
-            d_.copy_(h_, non_blocking=True)
-        step()
-        for h_, d_ in zip(hout, (dq, dk, dv)):
-            h_.copy_(d_, non_blocking=True)
+        for c, (a, b) in enumerate(bounds):
+            r0, r1 = a * per, b * per
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_out[c])  # the previous step is done with this chunk's buffers
+                for d_, h_ in zip(din, hinf):
+                    d_[r0:r1].copy_(h_[r0:r1], non_blocking=True)
+                ev_in[c].record(s_in)
+            stream.wait_event(ev_in[c])
+            if w.B > 1:
+                Bc, Hc, klc = b - a, w.H, (kl[a:b] if kl is not None else None)
+            else:
+                Bc, Hc, klc = 1, b - a, kl
+            qc, kc, vc, oc, doc, lc = (t_[r0:r1] for t_ in din)
+            dqc, dkc, dvc = (t_[r0:r1] for t_ in dout_)
+            if args.window:
+                st = sdp.attn_bwd_window(qc, kc, vc, oc, doc, lc, dqc, dkc, dvc, Bc, Hc, w.N, w.d, w.scale, w.causal,
+                                         klc, args.window, wsbuf, nbytes, sh)
+            else:
+                st = sdp.attn_bwd(qc, kc, vc, oc, doc, lc, dqc, dkc, dvc, Bc, Hc, w.N, w.d, w.scale, w.causal, klc,
+                                  wsbuf, nbytes, sh)
+            if st != sdp.ATTN_OK:
+                raise sdp.AttnError(st, "attn_bwd")
+            ev_done[c].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[c])
+                for h_, d_ in zip(houtf, dout_):
+                    h_[r0:r1].copy_(d_[r0:r1], non_blocking=True)
+                ev_out[c].record(s_out)
 
-    for _ in range(3):
+    for _ in range(2):
         e2e_step()
     torch.cuda.synchronize()
     e2, e3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2.record(stream)
+    e2.record(s_in)
     for _ in range(args.e2e_steps):
         e2e_step()
-    e3.record(stream)
+    e3.record(s_out)
     torch.cuda.synchronize()
+    # dK and dV are accumulated in a fixed order: the chunked calls must match
+    # the whole-problem call bit for bit (dQ adds in no fixed order).
+    if not (torch.equal(hout[1].cuda(), ref_dk) and torch.equal(hout[2].cuda(), ref_dv)):
+        raise RuntimeError("end-to-end dK/dV differ from the device-resident run")
     ms_e2e = max_over_ranks(e2.elapsed_time(e3) / args.e2e_steps, ws, "cuda")
     peaks = measured_peaks()
     flops = 2.5 * (window_flops(w, args.window) if args.window else w.flops())
@@ -550,6 +597,7 @@ def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
                 "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in hin),
                 "d2h_bytes_per_step": sum(h.numel() * h.element_size() for h in hout), "ms_per_step": ms_e2e},
         "gpu_launches": 3 * args.steps,
+        "e2e_launches_per_step": 3 * len(bounds),
         "clocks": sampler.summary(),
         "kernel_src_sha": kernel_source_sha("bwd"),
     }
