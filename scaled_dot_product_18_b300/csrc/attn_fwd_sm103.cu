@@ -72,6 +72,11 @@ constexpr uint32_t kTmemO = 256;   // O_t at kTmemO + t * D
 // exceeds it by more than 2^8, so P stays <= 256 and O needs a rescale only
 // rarely.  Exact: O and l always share the same stale max.
 constexpr float kRescaleThreshold = 8.0f;
+// Within a key tile the max is settled from the first 64 score columns; the
+// second half moves it only past this margin (P <= 2^32 otherwise, exact in
+// the fp32 sums and the bf16 P), since moving it there means rescaling the
+// first half's P, already stored as bf16, a second rounding.
+constexpr float kInTileLimit = 32.0f;
 
 template <int D>
 struct Smem {
@@ -404,29 +409,93 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             };
 
-            // Pass 1: the row max of this tile.  S is read twice from TMEM
-            // instead of being held in 128 registers.
-            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            // One pass over S: each 64-column half is loaded from TMEM once,
+            // its max taken and its P formed against the running max m, which
+            // the first half moves when a score passes it by more than the
+            // lazy threshold.  The second half moves it only past
+            // kInTileLimit; then the first half's stored P and its sums are
+            // scaled by 2^(m_before - m) in place.
+            struct Sums {
+                float2 a0, a1;  // fp32 sums of P (two chains)
+                float r[4];     // sums of P as rounded to bf16
+            };
+            auto exp_pack = [&](const uint32_t (&r)[32], uint32_t p_col, float2 nm2, Sums &sm) {
+                uint32_t pk[16];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t ra[32], rb[32];
-                load64(64 * h, ra, rb);
+                for (int c = 0; c < 16; ++c) {
+                    const float2 x =
+                        __ffma2_rn(make_float2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sl2, nm2);
+                    const float2 p = make_float2(ex2(x.x), ex2(x.y));
+                    if (c & 1)
+                        sm.a1 = __fadd2_rn(sm.a1, p);
+                    else
+                        sm.a0 = __fadd2_rn(sm.a0, p);
+                    pk[c] = pack_bf16x2(p.x, p.y);
+                    add_bf16x2_f32(sm.r[2 * (c & 1)], sm.r[2 * (c & 1) + 1], pk[c]);
+                }
+                tmem_st16(tS + p_col, pk);
+            };
+            auto half_max = [&](const uint32_t (&ra)[32], const uint32_t (&rb)[32]) -> float {
+                float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     mx[c & 3] = fmax3(mx[c & 3], __uint_as_float(ra[2 * c]), __uint_as_float(ra[2 * c + 1]));
                     mx[c & 3] = fmax3(mx[c & 3], __uint_as_float(rb[2 * c]), __uint_as_float(rb[2 * c + 1]));
                 }
-            }
-            const float t_max = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
-            float alpha = 1.f;
-            if (t_max > m + kRescaleThreshold) {
-                alpha = ex2(m - t_max);  // 0 on the first tile (m = -inf)
-                m = t_max;
+                return fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * scale_log2;
+            };
+            const float m_old = m;
+            Sums sA = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), {0.f, 0.f, 0.f, 0.f}};
+            Sums sB = sA;
+            uint32_t ra[32], rb[32];
+            load64(0, ra, rb);
+            {
+                const float t0 = half_max(ra, rb);
+                if (t0 > m + kRescaleThreshold) m = t0;
             }
             // A row that has seen no visible key yet keeps m = -inf; its
             // scores are all -inf too, so any finite shift gives P = 0.
-            const float m_use = (kWindow && m == -INFINITY) ? 0.f : m;
-            const float2 nm2 = make_float2(-m_use, -m_use);
+            float m_use = m == -INFINITY ? 0.f : m;
+            exp_pack(ra, 0, make_float2(-m_use, -m_use), sA);
+            exp_pack(rb, 16, make_float2(-m_use, -m_use), sA);
+            // Second half: score columns 64..127, untouched by the P columns
+            // 0..31 written so far.
+            load64(64, ra, rb);
+            {
+                const float t1 = half_max(ra, rb);
+                const bool move = t1 > m + kInTileLimit;
+                // The TMEM loads and stores below are warp-collective: the
+                // whole warp takes the branch; rows whose max did not move
+                // rewrite their P unchanged (beta = 1 is exact).
+                if (__any_sync(0xffffffffu, move)) {
+                    const float beta = move ? ex2(m_use - t1) : 1.f;
+                    tmem_st_wait();
+                    uint32_t pr[32];
+                    tmem_ld32(tS, pr);
+                    tmem_ld_wait(pr);
+                    float r4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        pr[c] = pack_bf16x2(__uint_as_float(pr[c] << 16) * beta,
+                                            __uint_as_float(pr[c] & 0xFFFF0000u) * beta);
+                        add_bf16x2_f32(r4[2 * (c & 1)], r4[2 * (c & 1) + 1], pr[c]);
+                    }
+                    tmem_st32(tS, pr);
+                    if (move) {
+                        m = t1;
+                        m_use = t1;
+                        sA.r[0] = r4[0];
+                        sA.r[1] = r4[1];
+                        sA.r[2] = r4[2];
+                        sA.r[3] = r4[3];
+                        sA.a0 = make_float2(sA.a0.x * beta, sA.a0.y * beta);
+                        sA.a1 = make_float2(sA.a1.x * beta, sA.a1.y * beta);
+                    }
+                }
+            }
+            exp_pack(ra, 32, make_float2(-m_use, -m_use), sB);
+            exp_pack(rb, 48, make_float2(-m_use, -m_use), sB);
+            const float alpha = m != m_old ? ex2(m_old - m) : 1.f;  // 0 on the first visible tile
 
             // O_t += P_t V_{j-1} is complete (the S_t commit covers it), so O_t
             // can be rescaled here; rows whose max did not move keep alpha = 1.
@@ -441,41 +510,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(tO + c * 32, o);
                 }
             }
-
-            // Pass 2: P_t = 2^(s*scale*log2e - m) as bf16 pairs over the first
-            // 64 columns of S_t.  The P columns written for score columns
-            // [0, 64h+64) lie in [0, 32h+32): scores already read.
-            float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-            float rs[4] = {0.f, 0.f, 0.f, 0.f};
-            auto exp_pack = [&](const uint32_t (&r)[32], uint32_t p_col) {
-                uint32_t pk[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float2 x =
-                        __ffma2_rn(make_float2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1])), sl2, nm2);
-                    const float2 p = make_float2(ex2(x.x), ex2(x.y));
-                    if (c & 1)
-                        acc1 = __fadd2_rn(acc1, p);
-                    else
-                        acc0 = __fadd2_rn(acc0, p);
-                    pk[c] = pack_bf16x2(p.x, p.y);
-                    add_bf16x2_f32(rs[2 * (c & 1)], rs[2 * (c & 1) + 1], pk[c]);
-                }
-                tmem_st16(tS + p_col, pk);
-            };
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t ra[32], rb[32];
-                load64(64 * h, ra, rb);
-                exp_pack(ra, 32 * h);
-                exp_pack(rb, 32 * h + 16);
-            }
-            const float2 acc = __fadd2_rn(acc0, acc1);
+            const float2 acc = __fadd2_rn(__fadd2_rn(sA.a0, sA.a1), __fadd2_rn(sB.a0, sB.a1));
             l = fmaf(l, alpha, acc.x + acc.y);
             // O is normalised by the sum of the weights it was built from, so
             // O / l_o is a convex combination of V rows up to the bf16
             // rounding of their relative sizes.
-            l_o = fmaf(l_o, alpha, (rs[0] + rs[1]) + (rs[2] + rs[3]));
+            l_o = fmaf(l_o, alpha, ((sA.r[0] + sA.r[1]) + (sA.r[2] + sA.r[3])) + ((sB.r[0] + sB.r[1]) + (sB.r[2] + sB.r[3])));
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(bar(L::kBarPFull + t));
