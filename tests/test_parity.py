@@ -132,6 +132,37 @@ def test_large_logits_and_lazy_rescale():
         assert_close(O, lse, O_ref, lse_ref, "large logits causal=%s" % causal)
 
 
+@pytest.mark.parametrize("jump", [12.0, 30.0])
+def test_max_jump_inside_a_key_tile(jump):
+    # Within one 128-key tile the row max is settled from the first 64 keys;
+    # here keys 64..127 of the first tile (and of the third) score `jump`
+    # higher than keys 0..63 (log2 units: x 1.44).  jump 12: the second half
+    # stays below the in-tile margin, its weights reach ~2^17 and the next
+    # tile moves the max; jump 30: past the margin, the first half's stored
+    # weights are rescaled in place.  Rows differ (a per-row jump), so warps
+    # hold rows that do and rows that do not move.
+    from scaled_dot_product_18_b300.inputs import f64_to_bf16_bits
+    B, H, N, d = 1, 2, 384, 128
+    rng_q = oracle.bf16_to_f64(I.make_tensor_bits(23, 0, (B, H, N, d)))
+    rng_k = oracle.bf16_to_f64(I.make_tensor_bits(23, 1, (B, H, N, d)))
+    q = rng_q * 0.2
+    k = rng_k * 0.2
+    # unit direction e_0 carries the jump: q_i[0] = a_i, k_j[0] = 1 on the
+    # boosted keys, so s_ij gains a_i / sqrt(d) * sqrt(d) = a_i with scale 1/sqrt(d)
+    a = jump * (0.5 + 0.5 * (np.arange(N) % 2))  # half the rows jump fully, half by half
+    q[..., 0] = a[None, None, :] * np.sqrt(d)
+    boost = np.zeros(N)
+    boost[64:128] = 1.0
+    boost[320:384] = 1.0
+    k[..., 0] = boost[None, None, :]
+    qb, kb = f64_to_bf16_bits(q), f64_to_bf16_bits(k)
+    v = I.make_tensor_bits(23, 2, (B, H, N, d))
+    scale = 1.0 / np.sqrt(d)
+    O, lse = run_cuda(qb, kb, v, scale, False)
+    O_ref, lse_ref = oracle.attention_rows(qb, kb, v, scale, False)
+    assert_close(O, lse, O_ref, lse_ref, "in-tile max jump %.0f" % jump)
+
+
 def test_custom_scale_no_lse_and_side_stream():
     import torch
     B, H, N, d = 2, 3, 300, 128
