@@ -167,6 +167,24 @@ def test_backward_sampled_full_size(name):
         assert np.isfinite(G).all()
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_d64_long_sequence_sampled(causal):
+    # d = 64 (dQ staged in half a ring stage) over N = 4096 with key lengths.
+    B, H, N, d = 2, 2, 4096, 64
+    q, k, v, do = (I.make_tensor_bits(52, s, (B, H, N, d)) for s in (0, 1, 2, 4))
+    kl = np.array([N, 2500], dtype=np.int32)
+    got, O = run_bwd(q, k, v, do, 0.125, causal, kl, want_out=True)
+    rows = _sample(N, np.random.default_rng(8))
+    heads = [(0, 1), (1, 0)]
+    kw = dict(heads=heads, q_rows=rows, k_rows=rows)
+    ref = oracle.attention_backward_sampled(q, k, v, do, 0.125, causal, kl, **kw)
+    ref_stored = oracle.attention_backward_sampled(q, k, v, do, 0.125, causal, kl, out=O, **kw)
+    for (b, h) in heads:
+        check_grads([g[b, h, rows] for g in got], None, ref[(b, h)], ref_stored[(b, h)],
+                    "d64 N4096 causal=%s b%d h%d" % (causal, b, h))
+    assert (got[1][1, :, 2500:] == 0).all() and (got[2][1, :, 2500:] == 0).all()
+
+
 WINDOW_CASES = [(1, 129, 1), (2, 300, 64), (2, 300, 127), (2, 300, 129), (1, 700, 200), (2, 257, 300)]
 
 

@@ -58,6 +58,23 @@ def test_workload_sampled_parity(name):
     assert O.max() <= oracle.bf16_to_f64(x.v).max() + 1e-2 and O.min() >= oracle.bf16_to_f64(x.v).min() - 1e-2
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_d64_long_sequence_sampled(causal):
+    # The d = 64 instance (8-slot K/V ring) over many ring wraps: N = 8192,
+    # with key lengths on the second batch element; sampled rows.
+    B, H, N, d = 2, 3, 8192, 64
+    q, k, v = (I.make_tensor_bits(51, s, (B, H, N, d)) for s in (0, 1, 2))
+    kl = np.array([N, 5000], dtype=np.int32)
+    O, lse = run_cuda(q, k, v, 0.125, causal, kl)
+    rows = _sample_rows(N, np.random.default_rng(5))
+    for b, h in ((0, 0), (1, 2)):
+        O_ref, lse_ref = oracle.attention_rows(q[b:b + 1, h:h + 1], k[b:b + 1, h:h + 1], v[b:b + 1, h:h + 1], 0.125,
+                                               causal, kl[b:b + 1], rows=rows)
+        assert_close(O[b:b + 1, h:h + 1, rows], lse[b:b + 1, h:h + 1, rows], O_ref, lse_ref,
+                     "d64 N8192 causal=%s b%d h%d" % (causal, b, h))
+    assert np.isfinite(O).all() and np.isfinite(lse).all()
+
+
 EDGE_N = [1, 2, 63, 64, 65, 127, 128, 129, 255, 257]
 
 
