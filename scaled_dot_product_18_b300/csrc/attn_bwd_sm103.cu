@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -112,8 +113,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const __grid_constant__ CUtensorMap tm_dq, const float *__restrict__ stats,
                     __nv_bfloat16 *__restrict__ dk, __nv_bfloat16 *__restrict__ dv,
-                    const int32_t *__restrict__ key_lens, int H, int N, int n_tiles, int num_bh, float scale,
-                    float scale_log2, int causal, int window)
+                    const int32_t *__restrict__ key_lens, int H, int N, int n_tiles, int num_bh, int head_group,
+                    float scale, float scale_log2, int causal, int window)
 {
     using L = BwdSmem<D>;
     // The tiles are 128-byte swizzled and need a 1024-byte aligned base.  The
@@ -135,9 +136,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     // Key tiles in ascending order (the first ones see the most query tiles
-    // when causal), all heads of one key tile together.
-    const int bh = blockIdx.x % num_bh;
-    const int kt = static_cast<int>(blockIdx.x / num_bh);
+    // when causal), all heads of one key tile together -- within groups of
+    // head_group heads (all heads in one group unless the host chose smaller
+    // groups so that a group's q, k, v and dO stay in L2).
+    const int per_group = head_group * n_tiles;
+    const int grp = static_cast<int>(blockIdx.x / per_group);
+    const int g_heads = min(head_group, num_bh - grp * head_group);
+    const int in_grp = static_cast<int>(blockIdx.x) - grp * per_group;
+    const int bh = grp * head_group + in_grp % g_heads;
+    const int kt = in_grp / g_heads;
     const int b = bh / H, h = bh % H;
     int kv_len = N;
     if (key_lens != nullptr) kv_len = min(max(key_lens[b], 0), N);
@@ -536,10 +543,20 @@ int launch_bwd(const BwdLaunch &a)
         static_cast<const __nv_bfloat16 *>(a.out), static_cast<const __nv_bfloat16 *>(a.dout), a.lse, a.stats,
         a.dqacc, a.N, n_pad, rows_pad);
     if (cudaGetLastError() != cudaSuccess) return -1;
+    // Short heads: with key tile 0 of every head first, the running CTAs
+    // belong to as many different heads and each streams its own head's Q
+    // and dO from DRAM (B=4 H=32 N=4096: 148 heads, ~300 MB).  Groups of heads
+    // whose q, k, v, dO fit 24 MiB keep them in L2 (2.17 -> ~1.6 ms there);
+    // long heads keep the global order.
+    int head_group = num_bh;
+    if (n_tiles <= 32) {
+        const int64_t per_head = static_cast<int64_t>(a.N) * D * 2 * 4;
+        head_group = static_cast<int>(std::min<int64_t>(num_bh, std::max<int64_t>(1, (int64_t(24) << 20) / per_head)));
+    }
     attn_bwd_kernel<D><<<static_cast<unsigned>(n_tiles) * num_bh, kThreads, L::kBytes, a.stream>>>(
         *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, a.stats, static_cast<__nv_bfloat16 *>(a.dk),
-        static_cast<__nv_bfloat16 *>(a.dv), a.key_lens, a.H, a.N, n_tiles, num_bh, a.scale, a.scale * kLog2e,
-        a.causal, a.window);
+        static_cast<__nv_bfloat16 *>(a.dv), a.key_lens, a.H, a.N, n_tiles, num_bh, head_group, a.scale,
+        a.scale * kLog2e, a.causal, a.window);
     if (cudaGetLastError() != cudaSuccess) return -1;
     const int64_t n4 = static_cast<int64_t>(num_bh) * a.N * D / 4;
     bwd_finish<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, a.stream>>>(a.dqacc,
