@@ -543,16 +543,16 @@ int launch_bwd(const BwdLaunch &a)
         static_cast<const __nv_bfloat16 *>(a.out), static_cast<const __nv_bfloat16 *>(a.dout), a.lse, a.stats,
         a.dqacc, a.N, n_pad, rows_pad);
     if (cudaGetLastError() != cudaSuccess) return -1;
-    // Short heads: with key tile 0 of every head first, the running CTAs
-    // belong to as many different heads and each streams its own head's Q
-    // and dO from DRAM (B=4 H=32 N=4096: 148 heads, ~300 MB).  Groups of heads
-    // whose q, k, v, dO fit 24 MiB keep them in L2 (2.17 -> ~1.6 ms there);
-    // long heads keep the global order.
-    int head_group = num_bh;
-    if (n_tiles <= 32) {
-        const int64_t per_head = static_cast<int64_t>(a.N) * D * 2 * 4;
-        head_group = static_cast<int>(std::min<int64_t>(num_bh, std::max<int64_t>(1, (int64_t(24) << 20) / per_head)));
-    }
+    // With key tile 0 of every head first, the running CTAs spread over all
+    // heads: each streams its own head's Q and dO and adds into its own rows
+    // of the fp32 dQ accumulator, a working set far above L2 (B=4 H=32
+    // N=4096: ~148 heads; B=1 H=32 N=16384: 32 heads of 16 MiB plus 268 MB of
+    // accumulator).  Groups of heads whose q, k, v and dO fit 64 MiB keep
+    // most of it in L2: 2.17 -> 1.58 ms and 5.18 -> 4.79 ms on those shapes
+    // (2032 MHz).
+    const int64_t per_head = static_cast<int64_t>(a.N) * D * 2 * 4;
+    const int head_group =
+        static_cast<int>(std::min<int64_t>(num_bh, std::max<int64_t>(1, (int64_t(64) << 20) / per_head)));
     attn_bwd_kernel<D><<<static_cast<unsigned>(n_tiles) * num_bh, kThreads, L::kBytes, a.stream>>>(
         *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_do, *a.tm_dq, a.stats, static_cast<__nv_bfloat16 *>(a.dk),
         static_cast<__nv_bfloat16 *>(a.dv), a.key_lens, a.H, a.N, n_tiles, num_bh, head_group, a.scale,
