@@ -593,17 +593,16 @@ int launch(const AttnLaunch &a)
     const int num_q_pairs = (a.N + kRowsPerCta - 1) / kRowsPerCta;
     const int num_bh = a.B * a.H;
     const unsigned grid = static_cast<unsigned>(num_q_pairs) * static_cast<unsigned>(num_bh);
-    // Short heads (few query pairs each): with the heaviest-first order over
-    // all heads, the pairs of one head run in different waves and each
-    // re-reads the head's keys and values from DRAM (3.8x at B=4 H=32 N=4096
-    // d=128).  Ordering within groups of heads whose K/V fit in 24 MiB keeps
-    // them in L2 (+4 % there); long heads keep the global order, which
-    // balances the causal work better (-2 % with groups at N=16384).
-    int head_group = num_bh;
-    if (num_q_pairs <= 16) {
-        const int64_t kv_head = static_cast<int64_t>(a.N) * D * 2 * 2;
-        head_group = static_cast<int>(std::min<int64_t>(num_bh, std::max<int64_t>(1, (int64_t(24) << 20) / kv_head)));
-    }
+    // With the heaviest-first order over all heads, the running CTAs spread
+    // over every head and the pairs of one head run in different waves, each
+    // re-reading the head's keys and values from DRAM (3.8x the K/V bytes at
+    // B=4 H=32 N=4096 d=128).  Ordering heaviest-first within groups of heads
+    // whose K/V fit 32 MiB keeps them in L2: 0.506 -> ~0.46 ms there and
+    // 1.51 -> 1.46 ms at B=1 H=32 N=16384 (2032 MHz, measured with
+    // cool-downs; budgets of 64 and 128 MiB gave 1.47 and 1.48 ms).
+    const int64_t kv_head = static_cast<int64_t>(a.N) * D * 2 * 2;
+    const int head_group =
+        static_cast<int>(std::min<int64_t>(num_bh, std::max<int64_t>(1, (int64_t(32) << 20) / kv_head)));
     attn_fwd_kernel<D, kWindow><<<grid, kThreads, L::kAlloc, a.stream>>>(*a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, a.lse,
                                                                  a.key_lens, a.H, a.N, num_q_pairs, num_bh,
                                                                  head_group, a.scale_log2, a.causal, a.window);
