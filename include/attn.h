@@ -153,11 +153,16 @@ size_t attn_decode_workspace_size(int B, int H, int L, int d);
  * 8 MiB array of device memory that the library holds on every device that
  * loads it, for the life of the process.  The call allocates nothing.
  *
- * - Problems whose attn_decode_workspace_size exceeds 8 MiB return
- *   ATTN_ETOOLARGE before anything is launched (about 16,000 (batch, head)
- *   pairs at d = 128; use attn_decode with a caller workspace beyond that).
+ * - Arguments are checked exactly as attn_decode checks them, and in the
+ *   same order; only then do problems whose attn_decode_workspace_size
+ *   exceeds 8 MiB return ATTN_ETOOLARGE, before anything is launched (about
+ *   16,000 (batch, head) pairs at d = 128; use attn_decode with a caller
+ *   workspace beyond that).
  * - The first call on each device looks up that device's array address
  *   (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   The address is cached per device together with the id of the context it
+ *   was taken in; after cudaDeviceReset (a new context) the next call looks
+ *   it up again.
  * - Every call on a device shares the one array and leaves its partials in
  *   it.  Nothing in it needs clearing (each call writes every slot it reads),
  *   but calls that overlap on the GPU -- on different streams, or from
@@ -229,9 +234,10 @@ size_t attn_mha_workspace_size(int B, int N, int E);
  *           bytes, 16-byte aligned, overwritten by the call (an fp32 dQ
  *           accumulator and the D vector).
  * Three launches on `stream` (D and accumulator reset; one CTA per 128 keys
- * of one head accumulating dK, dV in tensor memory and adding dQ partials
- * with fp32 atomics; dQ conversion).  The order of the fp32 dQ additions is
- * not fixed, so dq may differ between runs in the last bf16 place.
+ * of one head accumulating dK, dV in tensor memory and adding its dQ partials
+ * into the fp32 accumulator with bulk tensor reduce-add copies; dQ
+ * conversion).  The order of the fp32 dQ additions is not fixed, so dq may
+ * differ between runs in the last bf16 place.
  */
 attn_status attn_bwd(const void *q, const void *k, const void *v, const void *out, const void *dout,
                      const float *lse, void *dq, void *dk, void *dv,
@@ -270,7 +276,22 @@ const char *attn_status_str(attn_status s);
 /* ABI version of this header (bumped on any signature change). */
 int attn_abi_version(void);
 
-#define ATTN_ABI_VERSION 5
+/*
+ * attn_tensor_map_cache_stats -- counters of the library's tensor-map cache.
+ *
+ * Every call describes its tensors to the TMA engine with tensor maps; an
+ * encoded map depends only on the buffer address, the sizes, strides and the
+ * tile shape, so the library keeps the last 256 distinct maps (a fixed table
+ * guarded by a mutex; nothing is allocated) and re-encodes only on a miss
+ * (see the latency-bound shapes of lshu.cn "Self-attention meets the compute
+ * wall", sec. 4.1: many small padded batches).  A caller that reuses its
+ * buffers pays a table lookup instead of up to five encodes per call.
+ * hits, misses: host pointers (either may be NULL) that receive the number of
+ * maps found in, and added to, the table since the library was loaded.
+ */
+void attn_tensor_map_cache_stats(uint64_t *hits, uint64_t *misses);
+
+#define ATTN_ABI_VERSION 6
 
 #ifdef __cplusplus
 }

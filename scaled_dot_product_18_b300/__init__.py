@@ -29,7 +29,7 @@ ATTN_ETOOLARGE = -6
 # Symbols declared in include/attn.h.
 EXPORTS = ("attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_workspace_size", "attn_decode_noalloc",
            "attn_mha_fwd", "attn_mha_workspace_size", "attn_bwd", "attn_bwd_window", "attn_bwd_workspace_size", "attn_check_device",
-           "attn_status_str", "attn_abi_version")
+           "attn_status_str", "attn_abi_version", "attn_tensor_map_cache_stats")
 
 _lib = None
 
@@ -77,6 +77,8 @@ def load_library():
     lib.attn_status_str.restype = ctypes.c_char_p
     lib.attn_abi_version.argtypes = []
     lib.attn_abi_version.restype = i
+    lib.attn_tensor_map_cache_stats.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]
+    lib.attn_tensor_map_cache_stats.restype = None
     _lib = lib
     return lib
 
@@ -235,6 +237,13 @@ def attn_status_str(status: int) -> str:
 
 def attn_abi_version() -> int:
     return load_library().attn_abi_version()
+
+
+def attn_tensor_map_cache_stats() -> tuple[int, int]:
+    """(hits, misses) of the library's tensor-map cache since it was loaded."""
+    h, m = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    load_library().attn_tensor_map_cache_stats(ctypes.byref(h), ctypes.byref(m))
+    return int(h.value), int(m.value)
 
 
 def attention(q, k, v, causal: bool = False, key_lens=None, scale: float | None = None, stream=None,

@@ -41,23 +41,97 @@ struct Strides {
     int64_t row, head, batch;
 };
 
+// ------------------------------------------------------------- tensor-map cache
+//
+// Encoding a tensor map costs about 1.5 us of host time, and a call encodes up
+// to five; at the small shapes that is more than the kernel takes.  A map is
+// a pure function of its encode arguments (address, type, sizes, strides,
+// box, swizzle), so maps are kept in a fixed table keyed on all of them and
+// copied out on a hit: a reused buffer layout costs a lookup, a new address
+// or shape one encode.  The table never allocates; when full, the oldest
+// entry is replaced.
+struct MapKey {
+    uint64_t base;
+    uint64_t dims[4];
+    uint64_t strides[3];
+    uint32_t box[4];
+    uint32_t rank, dtype, swizzle;
+    bool operator==(const MapKey &o) const
+    {
+        if (base != o.base || rank != o.rank || dtype != o.dtype || swizzle != o.swizzle) return false;
+        for (int i = 0; i < 4; ++i)
+            if (dims[i] != o.dims[i] || box[i] != o.box[i]) return false;
+        for (int i = 0; i < 3; ++i)
+            if (strides[i] != o.strides[i]) return false;
+        return true;
+    }
+};
+
+constexpr int kMapCacheSize = 256;
+struct MapCache {
+    std::mutex mu;
+    MapKey key[kMapCacheSize];
+    CUtensorMap map[kMapCacheSize];
+    int used = 0, next = 0;
+    uint64_t hits = 0, misses = 0;
+};
+MapCache &map_cache()
+{
+    static MapCache c;
+    return c;
+}
+
+// Encodes (or fetches from the cache) a tiled map of `rank` dimensions.
+bool cached_encode(CUtensorMap *m, CUtensorMapDataType dtype, uint32_t rank, const void *base, const cuuint64_t *dims,
+                   const cuuint64_t *strides, const cuuint32_t *box, CUtensorMapSwizzle swizzle)
+{
+    MapKey k{};
+    k.base = reinterpret_cast<uint64_t>(base);
+    k.rank = rank;
+    k.dtype = static_cast<uint32_t>(dtype);
+    k.swizzle = static_cast<uint32_t>(swizzle);
+    for (uint32_t i = 0; i < rank; ++i) {
+        k.dims[i] = dims[i];
+        k.box[i] = box[i];
+        if (i + 1 < rank) k.strides[i] = strides[i];
+    }
+    MapCache &c = map_cache();
+    {
+        std::lock_guard<std::mutex> lock(c.mu);
+        for (int i = 0; i < c.used; ++i)
+            if (c.key[i] == k) {
+                *m = c.map[i];
+                ++c.hits;
+                return true;
+            }
+    }
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (enc(m, dtype, rank, const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lock(c.mu);
+    ++c.misses;
+    const int slot = c.used < kMapCacheSize ? c.used++ : c.next;
+    c.next = (slot + 1) % kMapCacheSize;
+    c.key[slot] = k;
+    c.map[slot] = *m;
+    return true;
+}
+
 // 4-D view {d, N, H, B} of a bf16 tensor with the given element strides,
 // box = 64 head-dim columns x 128 rows x 1 head x 1 batch, 128-byte swizzle
 // (one box row = 128 bytes).  Rows past N read as zeros and are clipped on
 // store, so ragged N needs no padding.
 bool make_map(CUtensorMap *m, const void *base, int B, int H, int N, int d, Strides st)
 {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.row) * 2, static_cast<cuuint64_t>(st.head) * 2,
                                    static_cast<cuuint64_t>(st.batch) * 2};
     const cuuint32_t box[4] = {64, 128, 1, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return cached_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // Contiguous [B, H, N, d].
@@ -301,15 +375,10 @@ namespace {
 // rows, 128-byte swizzle): the target of the backward's TMA reductions.
 bool make_dq_map(CUtensorMap *m, float *base, int64_t BH, int N, int d)
 {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4, static_cast<cuuint64_t>(N) * d * 4};
     const cuuint32_t box[3] = {32, 32, 1};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return cached_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace
@@ -416,5 +485,13 @@ const char *attn_status_str(attn_status s)
 }
 
 int attn_abi_version(void) { return ATTN_ABI_VERSION; }
+
+void attn_tensor_map_cache_stats(uint64_t *hits, uint64_t *misses)
+{
+    MapCache &c = map_cache();
+    std::lock_guard<std::mutex> lock(c.mu);
+    if (hits) *hits = c.hits;
+    if (misses) *misses = c.misses;
+}
 
 }  // extern "C"

@@ -20,6 +20,7 @@
 //                   exp(lse_s - lse) O_s (the log-sum-exp merge of
 //                   aicoding.csdn.net "Why does attention stall large-model
 //                   training", sec. 2.2, chunked logsumexp), bf16 out.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -201,12 +202,25 @@ int launch_decode(const DecodeLaunch &a)
 
 }  // namespace
 
+// Streaming multiprocessors of the current device (148 on a B300 when no
+// device can be queried, e.g. for a size query on a host without a GPU).
+int sm_count()
+{
+    int dev = -1, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        n <= 0) {
+        (void)cudaGetLastError();  // the failed query must not surface at the next launch
+        return 148;
+    }
+    return n;
+}
+
 DecodeSplit decode_split(int B, int H, int L)
 {
     // Enough CTAs for every SM to keep many 16-byte loads in flight: about
     // sixteen per SM, each split at least 256 keys, chunks a multiple of 64.
     const int64_t heads = static_cast<int64_t>(B) * H;
-    const int64_t target = 148 * 16;
+    const int64_t target = static_cast<int64_t>(sm_count()) * 16;
     int64_t splits = (target + heads - 1) / heads;
     const int64_t max_splits = (static_cast<int64_t>(L) + 255) / 256;
     if (splits > max_splits) splits = max_splits;
@@ -249,18 +263,54 @@ constexpr int kMaxDevices = 64;
 // identifies the symbol, so its device address is fetched below.
 static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
 
-// Device address of g_decode_scratch on the current device, or nullptr.
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// Process-unique id of the current CUDA context (0 if it cannot be read).
+// cudaDeviceReset destroys a device's primary context and reloads the
+// library's module in the next one, which moves g_decode_scratch; context ids
+// are never reused, so a cached address is valid only for the id it was
+// taken under.
+unsigned long long current_context_id()
+{
+    static std::once_flag once;
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+// Device address of g_decode_scratch on the current device, or nullptr.  The
+// address is looked up once per device and context (the first call after the
+// device's context was created does it) and cached.
 void *static_scratch()
 {
     static std::mutex mu;
     static void *addr[kMaxDevices] = {};
+    static unsigned long long ctx_id[kMaxDevices] = {};
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    const unsigned long long id = current_context_id();  // 0 before the thread's first CUDA call
     std::lock_guard<std::mutex> lock(mu);
-    if (addr[dev] == nullptr) {
+    if (addr[dev] == nullptr || id == 0 || ctx_id[dev] != id) {
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
         addr[dev] = p;
+        ctx_id[dev] = current_context_id();  // the lookup has made the device's context current
     }
     return addr[dev];
 }
@@ -272,9 +322,16 @@ extern "C" attn_status attn_decode_noalloc(const void *q, const void *k_cache, c
                                            float *lse, int B, int H, int L, int d, float scale,
                                            const int32_t *cache_lens, attn_stream_t stream)
 {
+    // attn_decode's own argument checks come first, so that both entry points
+    // return the same status for the same bad argument; only a valid problem
+    // that does not fit the fixed area gets ATTN_ETOOLARGE.
     if (B < 0 || H < 0 || L < 0) return ATTN_EINVAL;
     if (d != 64 && d != 128) return ATTN_EUNSUPPORTED;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_EINVAL;
     if (B == 0 || H == 0) return ATTN_OK;
+    if (!q || !out) return ATTN_EINVAL;
+    if (static_cast<int64_t>(B) * H > INT32_MAX / 64) return ATTN_EINVAL;
+    if (L > 0 && (!k_cache || !v_cache)) return ATTN_EINVAL;
     const size_t need = attn_decode_workspace_size(B, H, L > 0 ? L : 1, d);
     if (need == 0) return ATTN_EINVAL;
     if (need > sdp18::kStaticScratchBytes) return ATTN_ETOOLARGE;

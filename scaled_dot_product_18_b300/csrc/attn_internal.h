@@ -23,6 +23,10 @@ struct AttnLaunch {
 // 0 on success, -1 on a CUDA error, -2 for an unsupported head dimension.
 int attn_fwd_launch(const AttnLaunch &a);
 
+// Streaming multiprocessors of the current device (148 when it cannot be
+// queried, e.g. a size query on a host without a GPU).
+int sm_count();
+
 // Decode (one query per (b, h) against a K/V cache of L rows).
 struct DecodeSplit {
     int splits;  // cache chunks per (b, h)

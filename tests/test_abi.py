@@ -32,14 +32,14 @@ def test_exports_every_declared_symbol(lib):
     assert {"attn_fwd", "attn_fwd_window", "attn_decode", "attn_decode_workspace_size", "attn_mha_fwd",
             "attn_mha_workspace_size", "attn_bwd", "attn_bwd_window", "attn_bwd_workspace_size", "attn_check_device",
             "attn_status_str",
-            "attn_abi_version"} <= names
+            "attn_abi_version", "attn_tensor_map_cache_stats"} <= names
     assert names == set(sdp.EXPORTS)
     for n in names:
         assert hasattr(lib, n), n
 
 
 def test_abi_version_and_status_strings(lib):
-    assert sdp.attn_abi_version() == 5
+    assert sdp.attn_abi_version() == 6
     for code in (0, -1, -2, -3, -4, -5):
         assert sdp.attn_status_str(code).startswith("ATTN_")
     assert sdp.attn_status_str(7) == "unknown attn_status"

@@ -23,6 +23,30 @@ def test_no_alloc_rejects_problems_beyond_its_scratch():
     assert "scratch" in sdp.attn_status_str(st)
 
 
+@pytest.mark.parametrize("args,want", [
+    (dict(scale=float("nan")), sdp.ATTN_EINVAL),
+    (dict(scale=0.0), sdp.ATTN_EINVAL),
+    (dict(q=None), sdp.ATTN_EINVAL),
+    (dict(out=None), sdp.ATTN_EINVAL),
+    (dict(k=None), sdp.ATTN_EINVAL),
+    (dict(d=96), sdp.ATTN_EUNSUPPORTED),
+    (dict(B=-1), sdp.ATTN_EINVAL),
+])
+def test_no_alloc_checks_arguments_before_the_size(args, want):
+    # A problem far too large for the fixed area (40,000 heads) with one bad
+    # argument gets the same status as attn_decode gives for that argument,
+    # not ATTN_ETOOLARGE; both are decided on the host (fake pointers).
+    P = 1 << 20
+    sdp.load_library()
+    a = dict(q=P, k=P, v=P, out=P, lse=None, B=40000, H=1, L=4096, d=128, scale=0.1, cl=None)
+    a.update(args)
+    order = ("q", "k", "v", "out", "lse", "B", "H", "L", "d", "scale", "cl")
+    st = sdp.attn_decode_noalloc(*(a[n] for n in order), None)
+    assert st == want, sdp.attn_status_str(st)
+    ws = sdp.attn_decode(*(a[n] for n in order), P, 1 << 30, None)
+    assert ws == want, sdp.attn_status_str(ws)
+
+
 @pytest.mark.gpu
 def test_no_alloc_matches_attn_decode_twice():
     import torch
