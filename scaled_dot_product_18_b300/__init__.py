@@ -47,7 +47,13 @@ def load_library():
         return _lib
     if not os.path.exists(LIB_PATH):
         raise RuntimeError("libattn.so is not built (%s); run __graft_entry__.build()" % LIB_PATH)
-    lib = ctypes.CDLL(LIB_PATH)
+    _lib = bind(ctypes.CDLL(LIB_PATH))
+    return _lib
+
+
+def bind(lib):
+    """Declare the argument and result types of every symbol of include/attn.h
+    on a loaded copy of the library; returns it."""
     vp, i = ctypes.c_void_p, ctypes.c_int
     lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, ctypes.c_float, i, vp, vp]
     lib.attn_fwd.restype = i
@@ -79,7 +85,6 @@ def load_library():
     lib.attn_abi_version.restype = i
     lib.attn_tensor_map_cache_stats.argtypes = [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64)]
     lib.attn_tensor_map_cache_stats.restype = None
-    _lib = lib
     return lib
 
 

@@ -23,25 +23,41 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+# The wait-timeout test library: the same sources compiled with
+# SDP18_WAIT_TEST (5 ms wait limit, a producer stall hook and two test-only
+# exports).  Only tests load it; the product library never contains the hook.
+WAIT_TEST_LIB = os.path.join(PKG, "libattn_waittest.so")
+
+
+def needs_build(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in SOURCES + HEADERS)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and not needs_build():
-        return LIB
-    tmp = LIB + ".tmp.%d" % os.getpid()
+def _compile(lib: str, defines: list[str], verbose: bool) -> str:
+    tmp = lib + ".tmp.%d" % os.getpid()
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc())), "lib64")
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", *defines,
            "-I" + INCLUDE, "-o", tmp, *SOURCES, "-lcublasLt", "-Xlinker", "-rpath=" + cuda_lib]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.check_call(cmd)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    if not force and not needs_build(LIB):
+        return LIB
+    return _compile(LIB, [], verbose)
+
+
+def build_wait_test(force: bool = False) -> str:
+    if not force and not needs_build(WAIT_TEST_LIB):
+        return WAIT_TEST_LIB
+    return _compile(WAIT_TEST_LIB, ["-DSDP18_WAIT_TEST"], False)
 
 
 if __name__ == "__main__":

@@ -56,6 +56,13 @@ namespace sdp18 {
 // Device error word of this library (read and cleared by the host).
 __device__ int g_sdp18_error = 0;
 
+#ifdef SDP18_WAIT_TEST
+// Test library only: when >= 0, the producer issues no K/V copy from this
+// ring item on, so the MMA warp's bounded wait for it runs out and the CTA
+// winds down (abort flag, error word, drain, TMEM freed).
+__device__ int g_test_stall_items = -1;
+#endif
+
 namespace {
 
 constexpr int kBM = 128;           // query rows per tile
@@ -215,6 +222,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         h, b);
             int issued = 0;
             for (int item = 0; item < 2 * n_max; ++item) {
+#ifdef SDP18_WAIT_TEST
+                if (g_test_stall_items >= 0 && item >= g_test_stall_items) break;
+#endif
                 const int s = item % L::kNumSlots;
                 const uint32_t round = static_cast<uint32_t>(item / L::kNumSlots);
                 if (!wait_warp(bar(L::kBarEmpty + s), (round & 1) ^ 1, 1)) break;
@@ -632,3 +642,18 @@ int read_and_clear_device_error(int *value)
 }
 
 }  // namespace sdp18
+
+#ifdef SDP18_WAIT_TEST
+// Test library only (not part of include/attn.h): set the stall item of the
+// forward's producer (-1 = none) and read the device error word without
+// clearing it.  Both return 0 on success.
+extern "C" int attn_test_set_stall(int items)
+{
+    return cudaMemcpyToSymbol(sdp18::g_test_stall_items, &items, sizeof(int)) == cudaSuccess ? 0 : -1;
+}
+
+extern "C" int attn_test_error_word(int *word)
+{
+    return cudaMemcpyFromSymbol(word, sdp18::g_sdp18_error, sizeof(int)) == cudaSuccess ? 0 : -1;
+}
+#endif

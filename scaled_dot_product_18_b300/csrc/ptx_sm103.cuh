@@ -105,18 +105,25 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 enum : int {
-    kErrWaitTimeout = 1,  // a bounded wait ran out; bits 8.. hold the wait site
+    kErrWaitTimeout = 1,  // a bounded wait ran out; bits 8.. hold the site of the first one
 };
 
 // Each wait gives up after this long; a whole forward launch takes
-// milliseconds, so reaching it means a lost arrival, never a slow GPU.
+// milliseconds, so reaching it means a lost arrival, never a slow GPU.  The
+// test library (built with SDP18_WAIT_TEST, never the product library) uses a
+// 5 ms limit so that a test can make a wait run out quickly.
+#ifdef SDP18_WAIT_TEST
+constexpr uint64_t kWaitLimitNs = 5000000ull;
+#else
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+#endif
 constexpr uint64_t kDrainLimitNs = 500000000ull;
 
 // Slow path of a bounded wait: spin with a time limit and an abort flag
-// shared by the CTA.  On timeout it raises the abort flag, ORs the error into
-// the library's device error word and returns false so the caller can wind
-// down.
+// shared by the CTA.  On timeout it raises the abort flag, records the error
+// in the library's device error word (the first wait to run out since the
+// word was cleared also records its site) and returns false so the caller
+// can wind down.
 __device__ __noinline__ inline bool wait_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag, int site,
                                               int *err_word)
 {
@@ -128,7 +135,7 @@ __device__ __noinline__ inline bool wait_slow(uint32_t bar, uint32_t parity, vol
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
-            atomicOr(err_word, kErrWaitTimeout | (site << 8));
+            if (atomicCAS(err_word, 0, kErrWaitTimeout | (site << 8)) != 0) atomicOr(err_word, kErrWaitTimeout);
             return false;
         }
     }
