@@ -147,15 +147,16 @@ attn_status launch_forward(const void *q, const void *k, const void *v, void *ou
                            int d, float scale, int causal, const int32_t *key_lens, int window, Strides in_st,
                            Strides out_st, attn_stream_t stream)
 {
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv;
     if (!make_map(&tq, q, B, H, N, d, in_st) || !make_map(&tk, k, B, H, N, d, in_st) ||
-        !make_map(&tv, v, B, H, N, d, in_st) || !make_map(&to, out, B, H, N, d, out_st))
+        !make_map(&tv, v, B, H, N, d, in_st))
         return ATTN_ECUDA;
     sdp18::AttnLaunch a{};
     a.tm_q = &tq;
     a.tm_k = &tk;
     a.tm_v = &tv;
-    a.tm_o = &to;
+    a.out = out;
+    a.ost = {out_st.row, out_st.head, out_st.batch};
     a.lse = lse;
     a.key_lens = key_lens;
     a.B = B;

@@ -9,9 +9,17 @@
 
 namespace sdp18 {
 
+// Element strides of the output's rows, heads and batches (row stride a
+// multiple of 8 elements: rows are written with 16-byte stores).
+struct OStrides {
+    int64_t row, head, batch;
+};
+
 struct AttnLaunch {
-    const CUtensorMap *tm_q, *tm_k, *tm_v, *tm_o;  // 3-D maps over [B*H, N, d] bf16
-    float *lse;                                    // [B*H*N] fp32 or nullptr
+    const CUtensorMap *tm_q, *tm_k, *tm_v;  // 4-D maps {d, N, H, B} bf16
+    void *out;                              // bf16 output, addressed through ost
+    OStrides ost;
+    float *lse;                             // [B*H*N] fp32 or nullptr
     const int32_t *key_lens;                       // [B] or nullptr
     int B, H, N, d;
     float scale_log2;  // scale * log2(e)
