@@ -206,12 +206,19 @@ int launch_decode(const DecodeLaunch &a)
 // device can be queried, e.g. for a size query on a host without a GPU).
 int sm_count()
 {
+    constexpr int kMaxDevices = 64;
+    static int cached[kMaxDevices] = {};  // 0 = not queried yet (benign race: every writer stores the same value)
     int dev = -1, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        n <= 0) {
+    if (cudaGetDevice(&dev) != cudaSuccess) {
         (void)cudaGetLastError();  // the failed query must not surface at the next launch
         return 148;
     }
+    if (dev >= 0 && dev < kMaxDevices && cached[dev] > 0) return cached[dev];
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        (void)cudaGetLastError();
+        return 148;
+    }
+    if (dev >= 0 && dev < kMaxDevices) cached[dev] = n;
     return n;
 }
 

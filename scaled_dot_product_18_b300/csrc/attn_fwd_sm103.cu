@@ -89,6 +89,7 @@ constexpr int kThreads = 320;      // 8 softmax warps + MMA warp + TMA warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;     // S_t at kTmemS + t * kBN
 constexpr uint32_t kTmemO = 256;   // O_t at kTmemO + t * D
+constexpr uint32_t kTmemP = 384;   // d = 64 only: P_t (packed bf16) at kTmemP + t * kBN / 2
 // Lazy rescaling: the running max used for P only moves when a row's true max
 // exceeds it by more than 2^8, so P stays <= 256 and O needs a rescale only
 // rarely.  Exact: O and l always share the same stale max.
@@ -114,13 +115,16 @@ struct Smem {
     static constexpr int kBarSFull = kBarEmpty + kNumSlots;  // [2]
     static constexpr int kBarPFull = kBarSFull + 2;          // [2]
     static constexpr int kBarODone = kBarPFull + 2;          // [2]
-    static constexpr int kBarDrain = kBarODone + 2;
+    static constexpr int kBarSFree = kBarODone + 2;          // [2] d = 64: S_t read into registers
+    static constexpr int kBarPVDone = kBarSFree + 2;         // [2] d = 64: O_t += P_t V done
+    static constexpr int kBarDrain = kBarPVDone + 2;
     static constexpr int kNumBars = kBarDrain + 1;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem address, abort flag
     static constexpr int kBytes = kOffMisc + 16;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
     static_assert(kTmemO + 2 * D <= kTmemCols, "TMEM budget");
+    static_assert(D != 64 || kTmemP == kTmemO + 2 * D, "d = 64 keeps P next to O");
 };
 
 // Key tiles [first, end) that query tile q0t visits; empty when first >= end.
@@ -209,6 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float scale_log2, int causal, int window)
 {
     using L = Smem<D>;
+    // At d = 64 the two O tiles leave 128 TMEM columns free: P_t gets its own
+    // columns, so S_t(j+1) need not wait for P_t(j) V_j (which reads P_t(j)
+    // out of S_t's columns at d = 128) and the softmax warps run from one key
+    // tile to the next without waiting for the tensor core.
+    constexpr bool kSplitP = D == 64;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t s_base = smem_addr(smem);
@@ -229,6 +238,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::kBarSFull + t), 1);
             mbar_init(bar(L::kBarPFull + t), 4 * 32);
             mbar_init(bar(L::kBarODone + t), 1);
+            mbar_init(bar(L::kBarSFree + t), 4 * 32);
+            mbar_init(bar(L::kBarPVDone + t), 1);
         }
         for (int s = 0; s < L::kNumSlots; ++s) {
             mbar_init(bar(L::kBarFull + s), 1);
@@ -336,8 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // 128 bytes per K step; the next 64 head-dim columns sit one
                 // [128 x 64] block further on (leading byte offset).
                 const uint64_t bd = sdesc_sw128(vbase + kk * 16 * 128, kBN * 128, 1024);
-                mma_bf16_ts_one(tm + kTmemO + t * D, tm + kTmemS + t * kBN + kk * 8, bd, kIdescPV,
-                                (acc || kk > 0) ? 1u : 0u);
+                const uint32_t a_tmem = kSplitP ? tm + kTmemP + t * (kBN / 2) + kk * 8 : tm + kTmemS + t * kBN + kk * 8;
+                mma_bf16_ts_one(tm + kTmemO + t * D, a_tmem, bd, kIdescPV, (acc || kk > 0) ? 1u : 0u);
             }
         };
         for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x)
@@ -367,7 +378,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (active(t, 0)) issue_s_q(t, ring % L::kNumSlots, n_t[t] == 1);
                 mma_commit_one(bar(L::kBarEmpty + ring % L::kNumSlots));
             }
-            if constexpr (!kWindow) {
+            if constexpr (kSplitP) {
+                // Per key tile: S_t(j+1) for each tile as soon as its softmax
+                // warps have read S_t(j), then P_t(j) V_j once they have stored
+                // P_t(j).  Covers the plain and the sliding-window kernel.
+                for (int j = 0; j < it.n_max && ok; ++j) {
+                    const int v_item = ring + 2 * j + 1, k_item = ring + 2 * j + 2;
+                    const int vs = v_item % L::kNumSlots, ks = k_item % L::kNumSlots;
+                    if (j + 1 < it.n_max) {  // K_{j+1} is streamed
+                        ok = wait_full(k_item, 7);
+                        for (int t = 0; t < 2 && ok; ++t) {
+                            if (!active(t, j + 1)) continue;
+                            // (A tile's first S of the item overwrites scores the
+                            // previous item's last P hand-off has released.)
+                            if (active(t, j)) {
+                                ok = wait_warp(bar(L::kBarSFree + t), (steps[t] + j - f_t[t]) & 1, 16 + t);
+                                if (!ok) break;
+                                tc_fence_after();
+                            }
+                            issue_s_q(t, ks, j + 2 - f_t[t] == n_t[t]);
+                        }
+                        if (!ok) break;
+                        mma_commit_one(bar(L::kBarEmpty + ks));
+                    }
+                    ok = wait_full(v_item, 4);
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        if (!active(t, j)) continue;
+                        const int jj = j - f_t[t];
+                        ok = wait_warp(bar(L::kBarPFull + t), (steps[t] + jj) & 1, 5 + t);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(t, vs, jj > 0);
+                        mma_commit_one(bar(L::kBarPVDone + t));
+                    }
+                    if (!ok) break;
+                    mma_commit_one(bar(L::kBarEmpty + vs));
+                }
+            } else if constexpr (!kWindow) {
                 // Both tiles start at key tile 0; tile 1 may run one tile longer.
                 for (int j = 0; j < it.n_max && ok; ++j) {
                     const int v_item = ring + 2 * j + 1, k_item = ring + 2 * j + 2;
@@ -447,6 +494,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t t_lane = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const uint32_t tS = t_lane + kTmemS + t * kBN;
         const uint32_t tO = t_lane + kTmemO + t * D;
+        // P_t goes over the first 64 score columns (d = 128) or to its own
+        // columns (d = 64).
+        const uint32_t tP = kSplitP ? t_lane + kTmemP + t * (kBN / 2) : tS;
         const float2 sl2 = make_float2(scale_log2, scale_log2);
         int step = 0;      // S_t / P_t phases used
         int o_done = 0;    // O_t phases used
@@ -529,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pk[c] = pack_bf16x2(p.x, p.y);
                         add_bf16x2_f32(sm.r[2 * (c & 1)], sm.r[2 * (c & 1) + 1], pk[c]);
                     }
-                    tmem_st16(tS + p_col, pk);
+                    tmem_st16(tP + p_col, pk);
                 };
                 auto half_max = [&](const uint32_t (&ra)[32], const uint32_t (&rb)[32]) -> float {
                     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -549,6 +599,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float t0 = half_max(ra, rb);
                     if (t0 > m + kRescaleThreshold) m = t0;
                 }
+                if constexpr (kSplitP) {
+                    // P_t(j-1) V_{j-1} must have read P_t and updated O_t before
+                    // P_t(j) is stored and O_t rescaled.
+                    if (jj > 0) {
+                        if (!wait_warp(bar(L::kBarPVDone + t), (step + jj - 1) & 1, 18 + t)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                }
                 // A row that has seen no visible key yet keeps m = -inf; its
                 // scores are all -inf too, so any finite shift gives P = 0.
                 float m_use = m == -INFINITY ? 0.f : m;
@@ -557,6 +618,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Second half: score columns 64..127, untouched by the P columns
                 // 0..31 written so far.
                 load64(64, ra, rb);
+                if constexpr (kSplitP) {
+                    // All of S_t(j) is in registers: S_t(j+1) may overwrite it.
+                    tc_fence_before();
+                    mbar_arrive(bar(L::kBarSFree + t));
+                }
                 {
                     const float t1 = half_max(ra, rb);
                     const bool move = t1 > m + kInTileLimit;
@@ -567,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const float beta = move ? ex2(m_use - t1) : 1.f;
                         tmem_st_wait();
                         uint32_t pr[32];
-                        tmem_ld32(tS, pr);
+                        tmem_ld32(tP, pr);
                         tmem_ld_wait(pr);
                         float r4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -576,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 __uint_as_float(pr[c] & 0xFFFF0000u) * beta);
                             add_bf16x2_f32(r4[2 * (c & 1)], r4[2 * (c & 1) + 1], pr[c]);
                         }
-                        tmem_st32(tS, pr);
+                        tmem_st32(tP, pr);
                         if (move) {
                             m = t1;
                             m_use = t1;
@@ -593,8 +659,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 exp_pack(rb, 48, make_float2(-m_use, -m_use), sB);
                 const float alpha = m != m_old ? ex2(m_old - m) : 1.f;  // 0 on the first visible tile
 
-                // O_t += P_t V_{j-1} is complete (the S_t commit covers it), so O_t
-                // can be rescaled here; rows whose max did not move keep alpha = 1.
+                // O_t += P_t V_{j-1} is complete (at d = 128 the S_t commit covers
+                // it, at d = 64 the wait above), so O_t can be rescaled here; rows
+                // whose max did not move keep alpha = 1.
                 if (jj > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
@@ -628,7 +695,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (q0t < N) {
                 const bool have = n_kv > 0;
                 if (have) {
-                    ok = wait_warp(bar(L::kBarODone + t), o_done & 1, 12 + t);
+                    // The item's last P V MMA: ODone (d = 128) or the last PVDone
+                    // phase (d = 64, step already counts this item's tiles).
+                    ok = kSplitP ? wait_warp(bar(L::kBarPVDone + t), (step - 1) & 1, 12 + t)
+                                 : wait_warp(bar(L::kBarODone + t), o_done & 1, 12 + t);
                     ++o_done;
                     tc_fence_after();
                     if (!ok) break;

@@ -131,10 +131,12 @@ def test_mask_probe_exact(d, causal):
     assert_close(O, lse, O_ref, lse_ref, "one-hot probe")
 
 
-def test_large_logits_and_lazy_rescale():
+@pytest.mark.parametrize("d", [64, 128])
+def test_large_logits_and_lazy_rescale(d):
     # Key norms grow along the sequence so each row's running max keeps rising
     # across key tiles (the rescale path), with logits far beyond exp's range.
-    B, H, N, d = 1, 4, 640, 128
+    # d = 64 keeps P in its own TMEM columns, d = 128 over the scores.
+    B, H, N = 1, 4, 640
     base_q = oracle.bf16_to_f64(I.make_tensor_bits(21, 0, (B, H, N, d)))
     base_k = oracle.bf16_to_f64(I.make_tensor_bits(21, 1, (B, H, N, d)))
     ramp = (1.0 + 6.0 * np.arange(N) / N)[None, None, :, None]
@@ -146,11 +148,12 @@ def test_large_logits_and_lazy_rescale():
         O, lse = run_cuda(q, k, v, 1.0 / np.sqrt(d), causal)
         O_ref, lse_ref = oracle.attention_rows(q, k, v, 1.0 / np.sqrt(d), causal)
         assert np.abs(lse_ref).max() > 50  # far outside exp's fp32 range without the max shift
-        assert_close(O, lse, O_ref, lse_ref, "large logits causal=%s" % causal)
+        assert_close(O, lse, O_ref, lse_ref, "large logits causal=%s d=%d" % (causal, d))
 
 
+@pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("jump", [12.0, 30.0])
-def test_max_jump_inside_a_key_tile(jump):
+def test_max_jump_inside_a_key_tile(jump, d):
     # Within one 128-key tile the row max is settled from the first 64 keys;
     # here keys 64..127 of the first tile (and of the third) score `jump`
     # higher than keys 0..63 (log2 units: x 1.44).  jump 12: the second half
@@ -159,7 +162,7 @@ def test_max_jump_inside_a_key_tile(jump):
     # weights are rescaled in place.  Rows differ (a per-row jump), so warps
     # hold rows that do and rows that do not move.
     from scaled_dot_product_18_b300.inputs import f64_to_bf16_bits
-    B, H, N, d = 1, 2, 384, 128
+    B, H, N = 1, 2, 384
     rng_q = oracle.bf16_to_f64(I.make_tensor_bits(23, 0, (B, H, N, d)))
     rng_k = oracle.bf16_to_f64(I.make_tensor_bits(23, 1, (B, H, N, d)))
     q = rng_q * 0.2
@@ -177,7 +180,7 @@ def test_max_jump_inside_a_key_tile(jump):
     scale = 1.0 / np.sqrt(d)
     O, lse = run_cuda(qb, kb, v, scale, False)
     O_ref, lse_ref = oracle.attention_rows(qb, kb, v, scale, False)
-    assert_close(O, lse, O_ref, lse_ref, "in-tile max jump %.0f" % jump)
+    assert_close(O, lse, O_ref, lse_ref, "in-tile max jump %.0f d=%d" % (jump, d))
 
 
 def test_custom_scale_no_lse_and_side_stream():
