@@ -204,6 +204,25 @@ def oracle_sample(w: I.Workload, x: I.HostInputs, budget_s: float, shape_hint=No
     return flops / dt, dt, desc, cores, (nh, nr)
 
 
+# ----------------------------------------------------------------- graph timing
+
+def capture_steps(step, steps: int):
+    """Record `steps` calls of step(stream_handle) into a CUDA graph on a side
+    stream.  Replaying it runs exactly the launches the direct calls would,
+    without the Python/ctypes time between them (the small workloads take
+    less GPU time per call than the host needs to issue one)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    cs = torch.cuda.Stream()
+    cs.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=cs):
+        for _ in range(steps):
+            step(cs.cuda_stream)
+    torch.cuda.current_stream().wait_stream(cs)
+    torch.cuda.synchronize()
+    return g
+
+
 # ----------------------------------------------------------------- main
 
 def max_over_ranks(ms: float, ws: int, device=None) -> float:
@@ -290,8 +309,8 @@ def run_decode(args, w: I.DecodeWorkload, ws: int, rank: int, local: int) -> int
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
 
-    def step():
-        st = sdp.attn_decode(q, k, v, out, lse, w.B, w.H, w.L, w.d, w.scale, cl, wsbuf, nbytes, sh)
+    def step(h=None):
+        st = sdp.attn_decode(q, k, v, out, lse, w.B, w.H, w.L, w.d, w.scale, cl, wsbuf, nbytes, h or sh)
         if st != sdp.ATTN_OK:
             raise sdp.AttnError(st, "attn_decode")
 
@@ -303,6 +322,7 @@ def run_decode(args, w: I.DecodeWorkload, ws: int, rank: int, local: int) -> int
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:  # noqa: BLE001
         uuid = None
+    graph = capture_steps(step, args.steps)  # the timed region replays these calls
     sampler = ClockSampler(uuid)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
@@ -310,8 +330,7 @@ def run_decode(args, w: I.DecodeWorkload, ws: int, rank: int, local: int) -> int
     torch.cuda.synchronize()
     with sampler:
         e0.record(stream)
-        for _ in range(args.steps):
-            step()
+        graph.replay()
         e1.record(stream)
         torch.cuda.synchronize()
     ms_step = max_over_ranks(e0.elapsed_time(e1), ws, "cuda") / args.steps
@@ -386,8 +405,8 @@ def run_mha(args, w: I.MhaWorkload, ws: int, rank: int, local: int) -> int:
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
 
-    def step():
-        st = sdp.attn_mha_fwd(tx, tw, to, out, lse, w.B, w.N, w.E, w.H, w.causal, kl, wsbuf, nbytes, sh)
+    def step(h=None):
+        st = sdp.attn_mha_fwd(tx, tw, to, out, lse, w.B, w.N, w.E, w.H, w.causal, kl, wsbuf, nbytes, h or sh)
         if st != sdp.ATTN_OK:
             raise sdp.AttnError(st, "attn_mha_fwd")
 
@@ -399,6 +418,7 @@ def run_mha(args, w: I.MhaWorkload, ws: int, rank: int, local: int) -> int:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:  # noqa: BLE001
         uuid = None
+    graph = capture_steps(step, args.steps)  # the timed region replays these calls
     sampler = ClockSampler(uuid)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
@@ -406,8 +426,7 @@ def run_mha(args, w: I.MhaWorkload, ws: int, rank: int, local: int) -> int:
     torch.cuda.synchronize()
     with sampler:
         e0.record(stream)
-        for _ in range(args.steps):
-            step()
+        graph.replay()
         e1.record(stream)
         torch.cuda.synchronize()
     ms_step = max_over_ranks(e0.elapsed_time(e1), ws, "cuda") / args.steps
@@ -482,13 +501,13 @@ def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
 
-    def step():
+    def step(h=None):
         if args.window:
             st = sdp.attn_bwd_window(q, k, v, out, do, lse, dq, dk, dv, w.B, w.H, w.N, w.d, w.scale, w.causal, kl,
-                                     args.window, wsbuf, nbytes, sh)
+                                     args.window, wsbuf, nbytes, h or sh)
         else:
             st = sdp.attn_bwd(q, k, v, out, do, lse, dq, dk, dv, w.B, w.H, w.N, w.d, w.scale, w.causal, kl, wsbuf,
-                              nbytes, sh)
+                              nbytes, h or sh)
         if st != sdp.ATTN_OK:
             raise sdp.AttnError(st, "attn_bwd")
 
@@ -500,6 +519,7 @@ def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:  # noqa: BLE001
         uuid = None
+    graph = capture_steps(step, args.steps)  # the timed region replays these calls
     sampler = ClockSampler(uuid)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if ws > 1:
@@ -507,8 +527,7 @@ def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
     torch.cuda.synchronize()
     with sampler:
         e0.record(stream)
-        for _ in range(args.steps):
-            step()
+        graph.replay()
         e1.record(stream)
         torch.cuda.synchronize()
     ms_step = max_over_ranks(e0.elapsed_time(e1), ws, "cuda") / args.steps
@@ -617,7 +636,7 @@ def main() -> int:
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=I.WORKLOAD_ORDER)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=I.WORKLOAD_ORDER + list(I.EXTRA_WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-oracle sample budget")
@@ -636,7 +655,7 @@ def main() -> int:
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    w = I.WORKLOADS[args.config]
+    w = I.WORKLOADS[args.config] if args.config in I.WORKLOADS else I.EXTRA_WORKLOADS[args.config]
     if args.batch is not None or args.heads is not None:
         B = w.B if args.batch is None else args.batch
         H = w.H if args.heads is None else args.heads
@@ -674,11 +693,12 @@ def main() -> int:
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
 
-    def step():
+    def step(h=None):
         if args.window:
-            st = sdp.attn_fwd_window(q, k, v, out, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, kl, args.window, sh)
+            st = sdp.attn_fwd_window(q, k, v, out, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, kl, args.window,
+                                     h or sh)
         else:
-            st = sdp.attn_fwd(q, k, v, out, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, kl, sh)
+            st = sdp.attn_fwd(q, k, v, out, lse, w.B, w.H, w.N, w.d, w.scale, w.causal, kl, h or sh)
         if st != sdp.ATTN_OK:
             raise sdp.AttnError(st)
 
@@ -698,13 +718,13 @@ def main() -> int:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:  # noqa: BLE001 - sample every visible GPU instead
         uuid = None
+    graph = capture_steps(step, args.steps)  # the timed region replays these calls
     sampler = ClockSampler(uuid)
     barrier()
     torch.cuda.synchronize()
     with sampler:
         e0.record(stream)
-        for _ in range(args.steps):
-            step()
+        graph.replay()
         e1.record(stream)
         torch.cuda.synchronize()
     barrier()
@@ -804,6 +824,7 @@ def main() -> int:
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "key_lens": list(w.key_len_range) if w.key_len_range else None,
                    "flops_per_step": flops, "parallelism": "replica per GPU" if ws > 1 else "single GPU",
+                   "timed": "one CUDA-graph replay of the %d attn_fwd calls" % args.steps,
                    "l2": "inputs larger than L2" if w.algorithmic_bytes() > 126e6 else "inputs fit in L2 (no flush)"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,

@@ -170,6 +170,12 @@ WORKLOADS = {
 }
 WORKLOAD_ORDER = list(WORKLOADS)
 
+# Further measured shapes: the B=4 H=32 N=4096 d=128 shape without the causal
+# mask (the non-causal, tensor-bound counterpart of the causal workloads).
+EXTRA_WORKLOADS = {
+    "c4nc_b4h32n4096d128": Workload("c4nc_b4h32n4096d128", 4, 32, 4096, 128, False),
+}
+
 
 def make_tensor_bits(seed: int, stream: int, shape: tuple[int, ...], amplitude: float = 1.0) -> np.ndarray:
     """bf16 bit patterns of N(0,1)*amplitude, C-contiguous, in ``shape``."""
