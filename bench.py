@@ -462,7 +462,7 @@ def run_mha(args, w: I.MhaWorkload, ws: int, rank: int, local: int) -> int:
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"], "traffic": None,
                      "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
-                     "kernel": "cuBLASLt projections + attn_fwd_kernel"},
+                     "kernel": "gemm_bf16_kernel (projections) + attn_fwd_kernel"},
         "e2e": {"value": job_tflops(w.flops(), ws, ms_e2e), "unit": "TFLOPS", "h2d_bytes_per_step": hx.numel() * 2,
                 "d2h_bytes_per_step": hout.numel() * 2, "ms_per_step": ms_e2e},
         "gpu_launches": args.steps,

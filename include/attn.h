@@ -195,12 +195,13 @@ attn_status attn_decode_noalloc(const void *q, const void *k_cache, const void *
  * key_lens: as in attn_fwd.  causal: as in attn_fwd.
  * workspace: caller-owned device memory of attn_mha_workspace_size(B, N, E)
  *          bytes (16-byte aligned) that the call overwrites: the bf16 Q/K/V
- *          rows, the merged heads and the GEMM library's scratch.
+ *          rows and the merged heads.
  * Q/K/V and M are bf16 tensors (fp32 accumulation, rounded to nearest even).
- * The projections run in cuBLASLt, the attention in this library's kernel,
+ * The two projections run on this library's tcgen05 GEMM kernel (128 x 256
+ * output tiles, persistent CTAs), the attention on its attention kernel,
  * which reads the heads straight out of the [B, N, 3E] rows through strided
- * tensor maps (no transpose kernels).  Asynchronous on `stream`; the only
- * allocation is cuBLASLt's host-side handle, created on the first call.
+ * tensor maps (no transpose kernels).  Three launches, asynchronous on
+ * `stream`; nothing is allocated.
  */
 attn_status attn_mha_fwd(const void *x, const void *w_qkv, const void *w_o, void *out, float *lse,
                          int B, int N, int E, int H, int causal, const int32_t *key_lens,

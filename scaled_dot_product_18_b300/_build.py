@@ -11,7 +11,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libattn.so")
 SOURCES = [os.path.join(CSRC, f) for f in ("attn_fwd_sm103.cu", "attn_bwd_sm103.cu", "attn_decode_sm103.cu",
-                                           "attn_api.cu")]
+                                           "gemm_sm103.cu", "attn_api.cu")]
 HEADERS = [os.path.join(CSRC, f) for f in ("ptx_sm103.cuh", "attn_internal.h")] + [os.path.join(INCLUDE, "attn.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -40,7 +40,7 @@ def _compile(lib: str, defines: list[str], verbose: bool) -> str:
     tmp = lib + ".tmp.%d" % os.getpid()
     cuda_lib = os.path.join(os.path.dirname(os.path.dirname(nvcc())), "lib64")
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared", *defines,
-           "-I" + INCLUDE, "-o", tmp, *SOURCES, "-lcublasLt", "-Xlinker", "-rpath=" + cuda_lib]
+           "-I" + INCLUDE, "-o", tmp, *SOURCES, "-Xlinker", "-rpath=" + cuda_lib]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.check_call(cmd)

@@ -1,7 +1,6 @@
 // C ABI of the attention forward: argument checks on the host, tensor-map
 // encoding, launch, and the device error word.  The operation and every
 // argument are specified in include/attn.h.
-#include <cublasLt.h>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -193,54 +192,35 @@ attn_status forward(const void *q, const void *k, const void *v, void *out, floa
 
 // ------------------------------------------------------------- multi-head block
 
-cublasLtHandle_t lt_handle()
+// 2-D view {inner, outer} of a row-major bf16 matrix with rows of `ld`
+// elements, 128-byte swizzled boxes of 64 x box_rows.
+bool make_map_2d(CUtensorMap *m, const void *base, int inner, int outer, int64_t ld, int box_rows)
 {
-    static std::once_flag once;
-    static cublasLtHandle_t h = nullptr;
-    std::call_once(once, [] {
-        if (cublasLtCreate(&h) != CUBLAS_STATUS_SUCCESS) h = nullptr;
-    });
-    return h;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(inner), static_cast<cuuint64_t>(outer)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    return cached_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
-// Column-major D[m x n] = A[m x k] * B[k x n] (leading dimensions m, k, m),
-// bf16 in and out, fp32 accumulation, on cuBLASLt with the given workspace.
-// A row-major product C = X * W is the column-major W^T X^T, so callers pass
-// the row-major operands as (A, B) = (W, X).
-bool gemm_bf16(int m, int n, int k, const void *A, const void *Bm, void *D, void *ws, size_t ws_bytes,
-               cudaStream_t stream)
+// C[M, N] = A[M, K] B[K, N], all row-major bf16 (leading dimensions K, N, N),
+// on this library's tcgen05 GEMM kernel.
+attn_status gemm_bf16(int M, int N, int K, const void *A, const void *Bm, void *C, cudaStream_t stream)
 {
-    cublasLtHandle_t h = lt_handle();
-    if (!h) return false;
-    cublasLtMatmulDesc_t op = nullptr;
-    cublasLtMatrixLayout_t la = nullptr, lb = nullptr, ld = nullptr;
-    cublasLtMatmulPreference_t pref = nullptr;
-    bool ok = cublasLtMatmulDescCreate(&op, CUBLAS_COMPUTE_32F, CUDA_R_32F) == CUBLAS_STATUS_SUCCESS &&
-              cublasLtMatrixLayoutCreate(&la, CUDA_R_16BF, m, k, m) == CUBLAS_STATUS_SUCCESS &&
-              cublasLtMatrixLayoutCreate(&lb, CUDA_R_16BF, k, n, k) == CUBLAS_STATUS_SUCCESS &&
-              cublasLtMatrixLayoutCreate(&ld, CUDA_R_16BF, m, n, m) == CUBLAS_STATUS_SUCCESS &&
-              cublasLtMatmulPreferenceCreate(&pref) == CUBLAS_STATUS_SUCCESS &&
-              cublasLtMatmulPreferenceSetAttribute(pref, CUBLASLT_MATMUL_PREF_MAX_WORKSPACE_BYTES, &ws_bytes,
-                                                   sizeof(ws_bytes)) == CUBLAS_STATUS_SUCCESS;
-    cublasLtMatmulHeuristicResult_t res{};
-    int n_res = 0;
-    if (ok)
-        ok = cublasLtMatmulAlgoGetHeuristic(h, op, la, lb, ld, ld, pref, 1, &res, &n_res) == CUBLAS_STATUS_SUCCESS &&
-             n_res > 0;
-    if (ok) {
-        const float alpha = 1.f, beta = 0.f;
-        ok = cublasLtMatmul(h, op, &alpha, A, la, Bm, lb, &beta, D, ld, D, ld, &res.algo, ws, ws_bytes, stream) ==
-             CUBLAS_STATUS_SUCCESS;
-    }
-    if (pref) cublasLtMatmulPreferenceDestroy(pref);
-    if (ld) cublasLtMatrixLayoutDestroy(ld);
-    if (lb) cublasLtMatrixLayoutDestroy(lb);
-    if (la) cublasLtMatrixLayoutDestroy(la);
-    if (op) cublasLtMatmulDescDestroy(op);
-    return ok;
+    CUtensorMap ta, tb;
+    if (!make_map_2d(&ta, A, K, M, K, 128) || !make_map_2d(&tb, Bm, N, K, N, 64)) return ATTN_ECUDA;
+    sdp18::GemmLaunch g{};
+    g.tm_a = &ta;
+    g.tm_b = &tb;
+    g.c = C;
+    g.ldc = N;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.stream = stream;
+    const int rc = sdp18::gemm_bf16_launch(g);
+    if (rc == -2) return ATTN_EUNSUPPORTED;
+    return rc == 0 ? ATTN_OK : ATTN_ECUDA;
 }
-
-constexpr size_t kGemmWorkspace = size_t(32) << 20;
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -252,7 +232,7 @@ size_t attn_mha_workspace_size(int B, int N, int E)
 {
     if (B <= 0 || N <= 0 || E <= 0) return 0;
     const size_t rows = static_cast<size_t>(B) * N;
-    return round256(rows * 3 * E * 2) + round256(rows * E * 2) + kGemmWorkspace;
+    return round256(rows * 3 * E * 2) + round256(rows * E * 2);
 }
 
 attn_status attn_mha_fwd(const void *x, const void *w_qkv, const void *w_o, void *out, float *lse, int B, int N,
@@ -276,22 +256,21 @@ attn_status attn_mha_fwd(const void *x, const void *w_qkv, const void *w_o, void
     const size_t qkv_bytes = round256(static_cast<size_t>(rows) * 3 * E * 2);
     auto *qkv = reinterpret_cast<__nv_bfloat16 *>(ws);
     auto *attn = reinterpret_cast<__nv_bfloat16 *>(ws + qkv_bytes);
-    void *gemm_ws = ws + qkv_bytes + round256(static_cast<size_t>(rows) * E * 2);
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
     // 1. [Q | K | V] = x W_qkv: rows of [B*N, 3E], head h at columns h*d of each part.
-    if (!gemm_bf16(3 * E, static_cast<int>(rows), E, w_qkv, x, qkv, gemm_ws, kGemmWorkspace, s)) return ATTN_ECUDA;
+    attn_status st = gemm_bf16(static_cast<int>(rows), 3 * E, E, x, w_qkv, qkv, s);
+    if (st != ATTN_OK) return st;
     // 2. Attention straight from the interleaved rows ([B, N, H, d] views), the
     //    merged heads written as rows of [B*N, E].
     const Strides in_st{3 * static_cast<int64_t>(E), d, static_cast<int64_t>(N) * 3 * E};
     const Strides out_st{E, d, static_cast<int64_t>(N) * E};
-    const attn_status st = launch_forward(qkv, qkv + E, qkv + 2 * E, attn, lse, B, H, N, d,
-                                          static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))), causal,
-                                          key_lens, 0, in_st, out_st, stream);
+    st = launch_forward(qkv, qkv + E, qkv + 2 * E, attn, lse, B, H, N, d,
+                        static_cast<float>(1.0 / std::sqrt(static_cast<double>(d))), causal, key_lens, 0, in_st,
+                        out_st, stream);
     if (st != ATTN_OK) return st;
     // 3. out = merged W_o.
-    if (!gemm_bf16(E, static_cast<int>(rows), E, w_o, attn, out, gemm_ws, kGemmWorkspace, s)) return ATTN_ECUDA;
-    return ATTN_OK;
+    return gemm_bf16(static_cast<int>(rows), E, E, attn, w_o, out, s);
 }
 
 
@@ -465,10 +444,11 @@ attn_status attn_bwd_window(const void *q, const void *k, const void *v, const v
 attn_status attn_check_device(attn_stream_t stream)
 {
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ECUDA;
-    int v = 0, vb = 0;
+    int v = 0, vb = 0, vg = 0;
     if (sdp18::read_and_clear_device_error(&v) != 0) return ATTN_ECUDA;
     if (sdp18::read_and_clear_bwd_error(&vb) != 0) return ATTN_ECUDA;
-    return (v != 0 || vb != 0) ? ATTN_EDEVICE : ATTN_OK;
+    if (sdp18::read_and_clear_gemm_error(&vg) != 0) return ATTN_ECUDA;
+    return (v != 0 || vb != 0 || vg != 0) ? ATTN_EDEVICE : ATTN_OK;
 }
 
 const char *attn_status_str(attn_status s)

@@ -76,6 +76,20 @@ struct BwdLaunch {
 // 0 on success, -1 on a CUDA error, -2 for an unsupported head dimension.
 int attn_bwd_launch(const BwdLaunch &a);
 
+// Dense bf16 GEMM C[M, N] = A[M, K] B[K, N] (row-major, fp32 accumulation,
+// bf16 out) for the multi-head block's projections.
+struct GemmLaunch {
+    const CUtensorMap *tm_a;  // 2-D {K, M} bf16, box 64 x 128, 128-byte swizzle
+    const CUtensorMap *tm_b;  // 2-D {N, K} bf16, box 64 x 64, 128-byte swizzle
+    void *c;                  // bf16 rows of ldc elements (16-byte aligned rows)
+    int64_t ldc;
+    int M, N, K;              // K a multiple of 64, N a multiple of 8
+    cudaStream_t stream;
+};
+// 0 on success, -1 on a CUDA error, -2 for unsupported sizes.
+int gemm_bf16_launch(const GemmLaunch &g);
+int read_and_clear_gemm_error(int *value);
+
 // Reads the device error word of the current device and clears it.
 int read_and_clear_device_error(int *value);
 // Same for the word the backward kernel writes.

@@ -194,6 +194,17 @@ __device__ __forceinline__ void tma_load_4d_one(uint32_t dst, const CUtensorMap 
         : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d_one(uint32_t dst, const CUtensorMap *map, uint32_t bar, int c0, int c1)
+{
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];\n\t}" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 // D(tmem) (+)= A(smem desc) * B(smem desc), kind::f16 (bf16 in, fp32 acc);
 // accumulate = 0 overwrites D.
 __device__ __forceinline__ void mma_bf16_ss_one(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
