@@ -19,9 +19,11 @@
 //                TMEM (its warp's lane quarter), rounds to bf16 and writes it
 //                with 16-byte stores, then frees the accumulator -- while the
 //                MMA warp already accumulates the next tile in the other one.
-// Tiles are visited in bands of 16 M-blocks (N blocks outer, M blocks inner
-// within a band), so the A rows and B columns the running CTAs share stay in
-// L2.  Rows past M and columns past N read as zero (TMA) and are not stored.
+// Tiles are visited in bands of M-blocks (N blocks outer, M blocks inner
+// within a band), the band sized so that its A rows (about 48 MB) stay in L2
+// while every column block of B streams past them once: B is read from DRAM
+// once per band, A once.  Rows past M and columns past N read as zero (TMA)
+// and are not stored.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -42,7 +44,6 @@ constexpr int kGM = 128;         // output rows per tile
 constexpr int kGN = 256;         // output columns per tile
 constexpr int kGK = 64;          // K per stage (one 128-byte swizzle row of bf16)
 constexpr int kStages = 4;
-constexpr int kBandM = 16;       // M blocks per raster band
 constexpr int kGThreads = 192;   // producer, MMA, 4 epilogue warps
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
@@ -67,18 +68,19 @@ struct GSmem {
 };
 
 // Output block (mb, nb) of tile t in the banded order.
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int &mb, int &nb)
+__device__ __forceinline__ void tile_coords(int t, int tiles_m, int tiles_n, int band_m, int &mb, int &nb)
 {
-    const int band = t / (kBandM * tiles_n);
-    const int r = t - band * kBandM * tiles_n;
-    const int rows = min(kBandM, tiles_m - band * kBandM);
+    const int band = t / (band_m * tiles_n);
+    const int r = t - band * band_m * tiles_n;
+    const int rows = min(band_m, tiles_m - band * band_m);
     nb = r / rows;
-    mb = band * kBandM + r % rows;
+    mb = band * band_m + r % rows;
 }
 
 __global__ void __launch_bounds__(kGThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                     __nv_bfloat16 *__restrict__ c, int64_t ldc, int M, int N, int K, int tiles_m, int tiles_n)
+                     __nv_bfloat16 *__restrict__ c, int64_t ldc, int M, int N, int K, int tiles_m, int tiles_n,
+                     int band_m)
 {
     using L = GSmem;
     extern __shared__ uint8_t smem_raw[];
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             int mb, nb;
-            tile_coords(t, tiles_m, tiles_n, mb, nb);
+            tile_coords(t, tiles_m, tiles_n, band_m, mb, nb);
             for (int kb = 0; kb < k_steps; ++kb, ++stage) {
                 const int s = stage % kStages;
                 if (!(ok = wait_warp(bar(L::kBarEmpty + s), ((stage / kStages) & 1) ^ 1, 40))) break;
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         bool ok = true;
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++tcount) {
             int mb, nb;
-            tile_coords(t, tiles_m, tiles_n, mb, nb);
+            tile_coords(t, tiles_m, tiles_n, band_m, mb, nb);
             const int acc = tcount & 1;
             if (!(ok = wait_warp(bar(L::kBarAccFull + acc), (tcount >> 1) & 1, 43))) break;
             tc_fence_after();
@@ -232,9 +234,12 @@ int gemm_bf16_launch(const GemmLaunch &g)
     const int tiles_m = (g.M + kGM - 1) / kGM, tiles_n = (g.N + kGN - 1) / kGN;
     const int64_t tiles = static_cast<int64_t>(tiles_m) * tiles_n;
     const unsigned grid = static_cast<unsigned>(std::min<int64_t>(tiles, sm_count()));
+    // M-blocks per band: their A rows (kGM x K bf16 each) within ~48 MB.
+    const int64_t a_block = static_cast<int64_t>(kGM) * g.K * 2;
+    const int band_m = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles_m, (int64_t(48) << 20) / a_block)));
     gemm_bf16_kernel<<<grid, kGThreads, GSmem::kAlloc, g.stream>>>(*g.tm_a, *g.tm_b,
                                                                     static_cast<__nv_bfloat16 *>(g.c), g.ldc, g.M,
-                                                                    g.N, g.K, tiles_m, tiles_n);
+                                                                    g.N, g.K, tiles_m, tiles_n, band_m);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
