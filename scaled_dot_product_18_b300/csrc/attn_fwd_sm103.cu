@@ -772,11 +772,23 @@ int launch(const AttnLaunch &a)
     const int64_t kv_head = static_cast<int64_t>(a.N) * D * 2 * 2;
     sc.head_group =
         static_cast<int>(std::min<int64_t>(sc.num_bh, std::max<int64_t>(1, (int64_t(32) << 20) / kv_head)));
-    sc.paired = a.causal && a.window == 0 && a.key_lens == nullptr ? 1 : 0;
-    const int per_head = sc.paired ? (sc.nqp + 1) / 2 : sc.nqp;
-    const int64_t units = static_cast<int64_t>(per_head) * sc.num_bh;
+    // Schedule.  Causal pairs cost 2p + 2 key tiles: pairing p with nqp-1-p
+    // makes equal units, which a static stride balances once there are a few
+    // per SM (long-context shape: 6.9 per SM, makespan 1.2 % over ideal in a
+    // simulation).  With fewer (e.g. 8 heads at N = 16384: 1.7 per SM, a
+    // whole unit of tail) or with key lengths, each CTA takes one item and
+    // the hardware hands CTAs to SMs as they free up (greedy, heaviest
+    // first).  Without the causal mask (or with a window) items cost about
+    // the same, and persistent CTAs striding over them keep set-up and drain
+    // off the tensor core.
+    const int sms = sm_count();
+    const int64_t items = static_cast<int64_t>(sc.nqp) * sc.num_bh;
+    const int64_t pair_units = static_cast<int64_t>((sc.nqp + 1) / 2) * sc.num_bh;
+    const bool causal_full = a.causal && a.window == 0;
+    sc.paired = causal_full && a.key_lens == nullptr && pair_units >= 4 * static_cast<int64_t>(sms) ? 1 : 0;
+    const int64_t units = sc.paired ? pair_units : items;
     // One CTA per SM (the kernel's shared memory and TMEM allow no more).
-    const unsigned grid = static_cast<unsigned>(std::min<int64_t>(units, sm_count()));
+    const unsigned grid = static_cast<unsigned>(causal_full && !sc.paired ? units : std::min<int64_t>(units, sms));
     attn_fwd_kernel<D, kWindow><<<grid, kThreads, L::kAlloc, a.stream>>>(
         *a.tm_q, *a.tm_k, *a.tm_v, static_cast<__nv_bfloat16 *>(a.out), a.ost, a.lse, a.key_lens, sc,
         static_cast<int>(units), a.scale_log2, a.causal, a.window);
