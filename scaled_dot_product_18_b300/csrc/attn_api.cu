@@ -120,16 +120,16 @@ bool cached_encode(CUtensorMap *m, CUtensorMapDataType dtype, uint32_t rank, con
 }
 
 // 4-D view {d, N, H, B} of a bf16 tensor with the given element strides,
-// box = 64 head-dim columns x 128 rows x 1 head x 1 batch, 128-byte swizzle
-// (one box row = 128 bytes).  Rows past N read as zeros and are clipped on
-// store, so ragged N needs no padding.
-bool make_map(CUtensorMap *m, const void *base, int B, int H, int N, int d, Strides st)
+// box = 64 head-dim columns x box_rows rows x 1 head x 1 batch, 128-byte
+// swizzle (one box row = 128 bytes).  Rows past N read as zeros and are
+// clipped on store, so ragged N needs no padding.
+bool make_map(CUtensorMap *m, const void *base, int B, int H, int N, int d, Strides st, int box_rows = 128)
 {
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.row) * 2, static_cast<cuuint64_t>(st.head) * 2,
                                    static_cast<cuuint64_t>(st.batch) * 2};
-    const cuuint32_t box[4] = {64, 128, 1, 1};
+    const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
     return cached_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -146,14 +146,15 @@ attn_status launch_forward(const void *q, const void *k, const void *v, void *ou
                            int d, float scale, int causal, const int32_t *key_lens, int window, Strides in_st,
                            Strides out_st, attn_stream_t stream)
 {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!make_map(&tq, q, B, H, N, d, in_st) || !make_map(&tk, k, B, H, N, d, in_st) ||
-        !make_map(&tv, v, B, H, N, d, in_st))
+        !make_map(&tv, v, B, H, N, d, in_st) || !make_map(&to, out, B, H, N, d, out_st, 32))
         return ATTN_ECUDA;
     sdp18::AttnLaunch a{};
     a.tm_q = &tq;
     a.tm_k = &tk;
     a.tm_v = &tv;
+    a.tm_o = &to;
     a.out = out;
     a.ost = {out_st.row, out_st.head, out_st.batch};
     a.lse = lse;

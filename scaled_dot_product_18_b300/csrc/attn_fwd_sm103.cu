@@ -107,7 +107,11 @@ struct Smem {
     static constexpr int kKVBytes = kBN * D * 2;  // one K or V tile
     static constexpr int kOffQ = 0;               // Q tile t at kOffQ + t * kQBytes
     static constexpr int kOffRing = kOffQ + kTilesPerCta * kQBytes;
-    static constexpr int kOffBar = kOffRing + kNumSlots * kKVBytes;
+    // d = 64 epilogue staging: each softmax warp's 32 rows x 64 columns (4 KB).
+    // (d = 128 has no room next to a 5-slot ring and stores O from registers.)
+    static constexpr int kOffStage = kOffRing + kNumSlots * kKVBytes;
+    static constexpr int kStageBytes = D == 64 ? 32 * 128 : 0;
+    static constexpr int kOffBar = kOffStage + 8 * kStageBytes;
     static constexpr int kBarQFull = 0;                      // [2] Q_t landed
     static constexpr int kBarQFree = 2;                      // [2] last S_t MMA of an item done
     static constexpr int kBarFull = 4;
@@ -208,7 +212,8 @@ __device__ __forceinline__ Item make_item(const Sched &sc, int qp, int bh, const
 template <int D, bool kWindow>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16 *__restrict__ out, OStrides ost,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    __nv_bfloat16 *__restrict__ out, OStrides ost,
                     float *__restrict__ lse, const int32_t *__restrict__ key_lens, Sched sc, int num_units,
                     float scale_log2, int causal, int window)
 {
@@ -688,10 +693,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             step += n_kv;
 
             // -------------------------------------------------------- epilogue
-            // O_t / l_o -> bf16, straight from registers to the output rows
-            // (16-byte stores; rows past N are not written).  The TMEM reads
-            // complete before this warp hands over the next item's P_t, so the
-            // next item's first P V MMA cannot overwrite O_t early.
+            // O_t / l_o -> bf16.  d = 64: 64 columns per warp go through the
+            // warp's own 4 KB of shared memory (128-byte swizzle) to one TMA
+            // store, which clips rows past N (coalesced: the item's tail is
+            // short at this size).  d = 128: 16-byte stores straight from
+            // registers (rows past N skipped).  The TMEM reads complete before
+            // this warp hands over the next item's P_t, so the next item's
+            // first P V MMA cannot overwrite O_t early.
             if (q0t < N) {
                 const bool have = n_kv > 0;
                 if (have) {
@@ -705,10 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // Rows with no visible key (l_o = 0) get O = 0 and lse = -inf.
                 const float inv_l = have && (!kWindow || l_o > 0.f) ? 1.f / l_o : 0.f;
-                __nv_bfloat16 *orow = out + static_cast<int64_t>(it.b) * ost.batch +
-                                      static_cast<int64_t>(it.h) * ost.head + static_cast<int64_t>(q_abs) * ost.row;
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
+                auto load_pack = [&](int c, uint32_t (&w)[16]) {
                     uint32_t o[32];
                     if (have) {
                         tmem_ld32(tO + c * 32, o);
@@ -717,14 +722,45 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] = 0u;
                     }
-                    uint32_t w[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-                    if (q_abs < N) {
+                };
+                if constexpr (D == 64) {
+                    const int lane = threadIdx.x & 31;
+                    const uint32_t stage = s_base + L::kOffStage + warp * L::kStageBytes;
+                    // The staging buffer is free once this warp's previous
+                    // store has read it.
+                    if (lane == 0) bulk_wait_read_all();
+                    __syncwarp();
+#pragma unroll
+                    for (int hc = 0; hc < 2; ++hc) {
+                        uint32_t w[16];
+                        load_pack(hc, w);
+                        // Row `lane`, 16-byte chunk u of 8: chunk index XOR (row % 8).
 #pragma unroll
                         for (int u = 0; u < 4; ++u)
-                            st_global_v4(orow + c * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                            st_shared_v4(stage + lane * 128 + (((4 * hc + u) ^ (lane & 7)) << 4), w[4 * u],
+                                         w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_4d(&tm_o, stage, 0, q0t + (warp & 3) * 32, it.h, it.b);
+                        tma_store_commit();
+                    }
+                } else {
+                    __nv_bfloat16 *orow = out + static_cast<int64_t>(it.b) * ost.batch +
+                                          static_cast<int64_t>(it.h) * ost.head + static_cast<int64_t>(q_abs) * ost.row;
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t w[16];
+                        load_pack(c, w);
+                        if (q_abs < N) {
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                st_global_v4(orow + c * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                        }
                     }
                 }
                 if (lse != nullptr && q_abs < N) {
@@ -734,6 +770,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
+        // Shared memory must outlive the warp's last O store (d = 64).
+        if (D == 64 && (threadIdx.x & 31) == 0) tma_store_wait_all();
+        __syncwarp();
         tc_fence_before();
     }
 
@@ -790,7 +829,7 @@ int launch(const AttnLaunch &a)
     // One CTA per SM (the kernel's shared memory and TMEM allow no more).
     const unsigned grid = static_cast<unsigned>(causal_full && !sc.paired ? units : std::min<int64_t>(units, sms));
     attn_fwd_kernel<D, kWindow><<<grid, kThreads, L::kAlloc, a.stream>>>(
-        *a.tm_q, *a.tm_k, *a.tm_v, static_cast<__nv_bfloat16 *>(a.out), a.ost, a.lse, a.key_lens, sc,
+        *a.tm_q, *a.tm_k, *a.tm_v, *a.tm_o, static_cast<__nv_bfloat16 *>(a.out), a.ost, a.lse, a.key_lens, sc,
         static_cast<int>(units), a.scale_log2, a.causal, a.window);
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }

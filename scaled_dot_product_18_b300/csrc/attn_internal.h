@@ -16,8 +16,9 @@ struct OStrides {
 };
 
 struct AttnLaunch {
-    const CUtensorMap *tm_q, *tm_k, *tm_v;  // 4-D maps {d, N, H, B} bf16
-    void *out;                              // bf16 output, addressed through ost
+    const CUtensorMap *tm_q, *tm_k, *tm_v;  // 4-D maps {d, N, H, B} bf16, 64 x 128 boxes
+    const CUtensorMap *tm_o;                // 4-D map {d, N, H, B} bf16, 64 x 32 boxes (d = 64 stores)
+    void *out;                              // the same output, addressed through ost (d = 128 stores)
     OStrides ost;
     float *lse;                             // [B*H*N] fp32 or nullptr
     const int32_t *key_lens;                       // [B] or nullptr
