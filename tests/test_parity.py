@@ -202,3 +202,22 @@ def test_deterministic():
     O2, l2 = run_cuda(q, k, v, 0.1, True)
     np.testing.assert_array_equal(O1, O2)
     np.testing.assert_array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_items_per_cta_with_empty_items(d, causal):
+    # 192 heads x 2 query pairs = 384 work items for at most one CTA per SM:
+    # without the causal mask each CTA walks two or three items, carrying its
+    # barrier phases, ring position and Q buffers from one to the next, and
+    # some items have no visible key at all (key length 0) or one.
+    B, H, N = 48, 4, 300
+    q, k, v = (I.make_tensor_bits(57 + d, s, (B, H, N, d)) for s in (0, 1, 2))
+    rng = np.random.default_rng(5 + d)
+    kl = rng.integers(0, N + 1, size=B).astype(np.int32)
+    kl[::7] = 0
+    kl[3::11] = 1
+    kl[5::13] = N
+    O, lse = run_cuda(q, k, v, 1.0 / np.sqrt(d), causal, kl)
+    O_ref, lse_ref = oracle.attention_rows(q, k, v, 1.0 / np.sqrt(d), causal, kl)
+    assert_close(O, lse, O_ref, lse_ref, "many items d=%d causal=%s" % (d, causal))
