@@ -47,6 +47,7 @@ KERNEL_SOURCES = {
     "fwd": ("attn_fwd_sm103.cu", "ptx_sm103.cuh", "attn_internal.h"),
     "bwd": ("attn_bwd_sm103.cu", "ptx_sm103.cuh", "attn_internal.h"),
     "decode": ("attn_decode_sm103.cu", "ptx_sm103.cuh", "attn_internal.h"),
+    "mha": ("attn_fwd_sm103.cu", "gemm_sm103.cu", "ptx_sm103.cuh", "attn_internal.h"),
 }
 
 
@@ -367,7 +368,7 @@ def run_decode(args, w: I.DecodeWorkload, ws: int, rank: int, local: int) -> int
         "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d,
                    "bytes_per_step": moved, "l2": "cache larger than L2" if moved > 126e6 else "fits in L2"},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": committed_traffic(w.name, "decode"),
                      "peak_source": peaks["source"] + " copy bandwidth (MEASURED_PEAKS.json)",
                      "kernel": "decode_partial + decode_combine"},
         "e2e": {"value": moved * ws / (ms_e2e * 1e-3) / 1e9, "unit": "GB/s",
@@ -465,9 +466,9 @@ def run_mha(args, w: I.MhaWorkload, ws: int, rank: int, local: int) -> int:
                      "kernel": "gemm_bf16_kernel (projections) + attn_fwd_kernel"},
         "e2e": {"value": job_tflops(w.flops(), ws, ms_e2e), "unit": "TFLOPS", "h2d_bytes_per_step": hx.numel() * 2,
                 "d2h_bytes_per_step": hout.numel() * 2, "ms_per_step": ms_e2e},
-        "gpu_launches": args.steps,
+        "gpu_launches": 3 * args.steps,  # QKV projection, attention, output projection
         "clocks": sampler.summary(),
-        "kernel_src_sha": kernel_source_sha(),
+        "kernel_src_sha": kernel_source_sha("mha"),
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
