@@ -100,6 +100,14 @@ constexpr float kRescaleThreshold = 8.0f;
 // first half's P, already stored as bf16, a second rounding.
 constexpr float kInTileLimit = 32.0f;
 
+// The producer warp works out each item of the CTA's schedule once and
+// publishes it in a small ring of shared-memory descriptors; the MMA and
+// softmax warps read it there instead of repeating the schedule arithmetic
+// (integer divisions, key ranges) at every item boundary.
+constexpr int kDescSlots = 4;
+constexpr int kDescBytes = 48;  // three int4: {q0, b, h, bh}, {kv_len, kr0, kr1.first}, {kr1.end, j_begin, n_max, valid}
+constexpr int kDescConsumers = 1 + 8;  // the MMA warp and the 8 softmax warps (one arrival per warp)
+
 template <int D>
 struct Smem {
     static constexpr int kNumSlots = D == 128 ? 5 : 8;
@@ -122,11 +130,15 @@ struct Smem {
     static constexpr int kBarSFree = kBarODone + 2;          // [2] d = 64: S_t read into registers
     static constexpr int kBarPVDone = kBarSFree + 2;         // [2] d = 64: O_t += P_t V done
     static constexpr int kBarDrain = kBarPVDone + 2;
-    static constexpr int kNumBars = kBarDrain + 1;
+    static constexpr int kBarDescFull = kBarDrain + 1;               // [kDescSlots] item published
+    static constexpr int kBarDescEmpty = kBarDescFull + kDescSlots;  // [kDescSlots] read by all consumers
+    static constexpr int kNumBars = kBarDescEmpty + kDescSlots;
     static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem address, abort flag
-    static constexpr int kBytes = kOffMisc + 16;
+    static constexpr int kOffDesc = (kOffMisc + 16 + 15) & ~15;  // kDescSlots item descriptors (int4 aligned)
+    static constexpr int kBytes = kOffDesc + kDescSlots * kDescBytes;
     static constexpr int kAlloc = kBytes + 1024;  // slack to align the base to 1024
     static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+    static_assert(kOffBar % 8 == 0 && kOffDesc % 16 == 0 && kDescBytes % 16 == 0, "barrier / descriptor alignment");
     static_assert(kTmemO + 2 * D <= kTmemCols, "TMEM budget");
     static_assert(D != 64 || kTmemP == kTmemO + 2 * D, "d = 64 keeps P next to O");
 };
@@ -251,6 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(L::kBarEmpty + s), 1);
         }
         mbar_init(bar(L::kBarDrain), 1);
+        for (int i = 0; i < kDescSlots; ++i) {
+            mbar_init(bar(L::kBarDescFull + i), 1);
+            mbar_init(bar(L::kBarDescEmpty + i), kDescConsumers);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -268,6 +284,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto wait_warp = [&](uint32_t b_addr, uint32_t parity, int site) -> bool {
         return __all_sync(0xffffffffu, wait_bounded(b_addr, parity, abort_flag, site, &g_sdp18_error));
     };
+    // Item descriptor k of this CTA: slot k % kDescSlots, phase k / kDescSlots.
+    auto desc_ptr = [&](int k) -> int4 * {
+        return reinterpret_cast<int4 *>(smem + L::kOffDesc + (k % kDescSlots) * kDescBytes);
+    };
+    // Consumer side (whole warp): wait for descriptor k, copy it, release the
+    // slot.  valid = false marks the end of the CTA's items.
+    auto read_desc = [&](int k, Item &it, bool &valid) -> bool {
+        if (!wait_warp(bar(L::kBarDescFull + k % kDescSlots), (k / kDescSlots) & 1, 9)) return false;
+        const int4 *dp = desc_ptr(k);
+        const int4 a = dp[0], c = dp[1], e = dp[2];
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0) mbar_arrive(bar(L::kBarDescEmpty + k % kDescSlots));
+        it.q0 = a.x;
+        it.b = a.y;
+        it.h = a.z;
+        it.bh = a.w;
+        it.kv_len = c.x;
+        it.kr[0] = {c.y, c.z};
+        it.kr[1] = {c.w, e.x};
+        it.n[0] = it.kr[0].count();
+        it.n[1] = it.kr[1].count();
+        it.j_begin = e.y;
+        it.n_max = e.z;
+        valid = e.w != 0;
+        return true;
+    };
 
     if (warp == kTmaWarp) {
         // ------------------------------------------------------------ producer
@@ -277,9 +319,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         int ring = 0;              // K/V copies issued so far (ring position)
         int q_loads[2] = {0, 0};   // Q_t copies issued so far
         bool ok = true;
+        int published = 0;  // item descriptors written
+        // Lane 0 writes descriptor `published` once its slot has been read by
+        // every consumer (kDescSlots items back).
+        auto publish = [&](const Item &it, int valid) -> bool {
+            const int k = published;
+            if (k >= kDescSlots &&
+                !wait_warp(bar(L::kBarDescEmpty + k % kDescSlots), ((k / kDescSlots) - 1) & 1, 14))
+                return false;
+            if ((threadIdx.x & 31) == 0) {
+                int4 *dp = desc_ptr(k);
+                dp[0] = make_int4(it.q0, it.b, it.h, it.bh);
+                dp[1] = make_int4(it.kv_len, it.kr[0].first, it.kr[0].end, it.kr[1].first);
+                dp[2] = make_int4(it.kr[1].end, it.j_begin, it.n_max, valid);
+                mbar_arrive(bar(L::kBarDescFull + k % kDescSlots));  // release: the stores are visible
+            }
+            __syncwarp();
+            ++published;
+            return true;
+        };
         for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x)
         for (int qps[2], bh_u, n_u = unit_pairs(sc, u, qps, bh_u), s_u = 0; s_u < n_u && ok; ++s_u) {
             const Item it = make_item(sc, qps[s_u], bh_u, key_lens, causal, window);
+            // Every item is published, also those with no key tile: their
+            // softmax warps still write O = 0 and lse = -inf.
+            if (!(ok = publish(it, 1))) break;
             if (it.n_max == 0) continue;
             // Q_t of this item goes where the previous item's Q_t was, once
             // that item's last S_t MMA has read it.
@@ -310,6 +374,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     (it.j_begin + (i >> 1)) * kBN, it.h, it.b);
                 ++ring;
             }
+        }
+        if (ok) {
+            Item end_it{};
+            publish(end_it, 0);
         }
         // Copies must have landed before the CTA's shared memory goes away.
         for (int t = 0; t < 2; ++t)
@@ -356,9 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_bf16_ts_one(tm + kTmemO + t * D, a_tmem, bd, kIdescPV, (acc || kk > 0) ? 1u : 0u);
             }
         };
-        for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x)
-        for (int qps[2], bh_u, n_u = unit_pairs(sc, u, qps, bh_u), s_u = 0; s_u < n_u && ok; ++s_u) {
-            const Item it = make_item(sc, qps[s_u], bh_u, key_lens, causal, window);
+        for (int k = 0; ok; ++k) {
+            Item it;
+            bool valid;
+            if (!(ok = read_desc(k, it, valid)) || !valid) break;
             if (it.n_max == 0) continue;
             const int n_t[2] = {it.n[0], it.n[1]};
             // Tile t is active at key tile j (0-based in the stream) when its
@@ -506,9 +575,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int step = 0;      // S_t / P_t phases used
         int o_done = 0;    // O_t phases used
         bool ok = true;
-        for (int u = blockIdx.x; u < num_units && ok; u += gridDim.x)
-        for (int qps[2], bh_u, n_u = unit_pairs(sc, u, qps, bh_u), s_u = 0; s_u < n_u && ok; ++s_u) {
-            const Item it = make_item(sc, qps[s_u], bh_u, key_lens, causal, window);
+        for (int k = 0; ok; ++k) {
+            Item it;
+            bool valid;
+            if (!(ok = read_desc(k, it, valid)) || !valid) break;
             const int q0t = it.q0 + t * kBM;
             const int q_abs = q0t + row;
             const int n_kv = it.n[t];
