@@ -100,6 +100,15 @@ constexpr float kRescaleThreshold = 8.0f;
 // first half's P, already stored as bf16, a second rounding.
 constexpr float kInTileLimit = 32.0f;
 
+// 32-byte store of eight 32-bit words (sm_100+; the address must be 32-byte
+// aligned).
+__device__ __forceinline__ void st_global_v8(void *p, const uint32_t *w)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // The producer warp works out each item of the CTA's schedule once and
 // publishes it in a small ring of shared-memory descriptors; the MMA and
 // softmax warps read it there instead of repeating the schedule arithmetic
@@ -176,6 +185,7 @@ struct Item {
 // group's keys and values stay in L2), heads innermost, heaviest pairs first.
 struct Sched {
     int H, N, nqp, num_bh, head_group, paired;
+    int o_v8;  // O's base and strides are 32-byte aligned: rows are written 32 bytes per store
 };
 
 // The query pairs of unit u (1 or 2, heaviest first) and its (batch, head).
@@ -827,9 +837,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint32_t w[16];
                         load_pack(c, w);
                         if (q_abs < N) {
+                            // Each thread writes its own row: 32-byte stores
+                            // fill whole L2 sectors, half as many requests as
+                            // 16-byte ones.
+                            if (sc.o_v8) {
+                                st_global_v8(orow + c * 32, w);
+                                st_global_v8(orow + c * 32 + 16, w + 8);
+                            } else {
 #pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                st_global_v4(orow + c * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                                for (int u = 0; u < 4; ++u)
+                                    st_global_v4(orow + c * 32 + u * 8, w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                                                 w[4 * u + 3]);
+                            }
                         }
                     }
                 }
@@ -867,6 +886,8 @@ int launch(const AttnLaunch &a)
         configured_device = dev;
     }
     Sched sc{};
+    sc.o_v8 = reinterpret_cast<uintptr_t>(a.out) % 32 == 0 && a.ost.batch % 16 == 0 && a.ost.head % 16 == 0 &&
+              a.ost.row % 16 == 0;
     sc.H = a.H;
     sc.N = a.N;
     sc.nqp = (a.N + kRowsPerCta - 1) / kRowsPerCta;

@@ -24,15 +24,18 @@ def to_dev(bits: np.ndarray):
     return t.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(t.bfloat16)
 
 
-def run_cuda(q_bits, k_bits, v_bits, scale, causal, key_lens=None, with_lse=True, stream=None, entry=None):
+def run_cuda(q_bits, k_bits, v_bits, scale, causal, key_lens=None, with_lse=True, stream=None, entry=None,
+             out_offset=0):
     """Run attn_fwd via the C ABI.  Returns (O float64 [B,H,N,d], lse float64
     [B,H,N] or None).  Outputs live inside larger buffers pre-filled with a
-    NaN canary; the guard zone after them is checked for stray writes."""
+    NaN canary; the guard zones around them are checked for stray writes.
+    out_offset (elements) moves O off the allocator's alignment."""
     t = torch()
     B, H, N, d = q_bits.shape
     q, k, v = to_dev(q_bits), to_dev(k_bits), to_dev(v_bits)
     n_out = B * H * N * d
-    out_buf = t.full((n_out + GUARD,), float("nan"), dtype=t.bfloat16, device="cuda")
+    out_alloc = t.full((out_offset + n_out + GUARD,), float("nan"), dtype=t.bfloat16, device="cuda")
+    out_buf = out_alloc[out_offset:]
     lse_buf = t.full((B * H * N + GUARD,), float("nan"), dtype=t.float32, device="cuda")
     kl = t.from_numpy(np.asarray(key_lens, dtype=np.int32)).cuda() if key_lens is not None else None
     fn = entry or sdp.attn_fwd
@@ -42,6 +45,7 @@ def run_cuda(q_bits, k_bits, v_bits, scale, causal, key_lens=None, with_lse=True
     assert sdp.attn_check_device(stream if stream is not None else t.cuda.current_stream()) == sdp.ATTN_OK
     tail = out_buf[n_out:].float()
     assert t.isnan(tail).all(), "stray write past the end of out"
+    assert t.isnan(out_alloc[:out_offset].float()).all(), "stray write before out"
     O = out_buf[:n_out].float().cpu().numpy().astype(np.float64).reshape(B, H, N, d)
     lse = None
     if with_lse:

@@ -195,6 +195,19 @@ def test_custom_scale_no_lse_and_side_stream():
     assert_close(O, None, O_ref, None, "scale 0.3, no lse, side stream")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_output_only_16_byte_aligned(d):
+    # O 16 bytes past a 512-byte boundary: the d = 128 epilogue falls back
+    # from 32-byte to 16-byte row stores, the d = 64 O tensor map starts
+    # off the usual alignment.
+    B, H, N = 2, 3, 333
+    q, k, v = (I.make_tensor_bits(57, s, (B, H, N, d)) for s in (0, 1, 2))
+    scale = 1.0 / np.sqrt(d)
+    O, lse = run_cuda(q, k, v, scale, True, out_offset=8)
+    O_ref, lse_ref = oracle.attention_rows(q, k, v, scale, True)
+    assert_close(O, lse, O_ref, lse_ref, "O at +16 bytes, d=%d" % d)
+
+
 def test_deterministic():
     B, H, N, d = 1, 4, 1000, 128
     q, k, v = (I.make_tensor_bits(41, s, (B, H, N, d)) for s in (0, 1, 2))
