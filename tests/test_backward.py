@@ -77,10 +77,13 @@ def assert_grad_close(G, R, what, rel_l2=REL_L2, max_rel=MAX_REL_TO_PEAK):
         assert rel <= rel_l2, "%s: rel-L2 %.3e" % (what, rel)
 
 
-def check_grads(got, O, ref_exact, ref_stored, what):
+def check_grads(got, O, ref_exact, ref_stored, what, peaked=True):
+    """peaked=False: no row is peaked (no causal mask, no key length below 64,
+    at least 64 keys), so dQ and dK meet the tight bounds against the exact D
+    as well."""
     for name, G, R, Rs in zip(("dQ", "dK", "dV"), got, ref_exact, ref_stored):
         assert_grad_close(G, Rs, "%s %s (D from the stored output)" % (name, what))
-        loose = name != "dV"
+        loose = name != "dV" and peaked
         assert_grad_close(G, R, "%s %s" % (name, what), rel_l2=PEAKED_REL_L2 if loose else REL_L2,
                           max_rel=2 * MAX_REL_TO_PEAK if loose else MAX_REL_TO_PEAK)
 
@@ -107,7 +110,8 @@ def test_backward_grid(d, causal):
         got, O = run_bwd(q, k, v, do, scale, causal, kla, want_out=True)
         ref = oracle.attention_backward_literal(q, k, v, do, scale, causal, kla)
         ref_stored = oracle.attention_backward_literal(q, k, v, do, scale, causal, kla, out=O)
-        check_grads(got, O, ref, ref_stored, "B%d H%d N%d d%d causal=%s kl=%s" % (B, H, N, d, causal, kl))
+        peaked = causal or N < 64 or (kl is not None and min(kl) < 64)
+        check_grads(got, O, ref, ref_stored, "B%d H%d N%d d%d causal=%s kl=%s" % (B, H, N, d, causal, kl), peaked)
         if kla is not None:
             for b in range(B):
                 # keys past the key length get exactly zero dK and dV
