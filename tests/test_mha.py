@@ -66,3 +66,33 @@ def test_mha_shapes(B, N, E, H, causal, lens):
     out, lse = run_mha(w, x)
     out_ref, lse_ref = oracle.mha_block(x.x, x.w_qkv, x.w_o, w.H, w.causal, x.key_lens)
     check(out, lse, out_ref, lse_ref, "B=%d N=%d E=%d H=%d" % (B, N, E, H))
+
+
+def test_mha_long_context_sampled():
+    # The long-context block at full size (B=1 N=16384 E=4096 H=32 causal), the
+    # launch the benchmark times.  The oracle follows the block's steps for
+    # sampled rows only: K and V for every key (one fp64 projection, rounded
+    # to bf16 as in the block), Q for the sampled rows, attention of those
+    # rows in every head, the merged row rounded to bf16, the output
+    # projection.  Rows are independent up to the attention, so this is the
+    # block oracle restricted to those rows.
+    w = I.MHA_WORKLOADS["mha_b1n16384e4096h32_causal"]
+    x = I.make_mha_inputs(w)
+    out, lse = run_mha(w, x)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    E, H, d, N = w.E, w.H, w.E // w.H, w.N
+    rows = np.array([0, 1, 127, 128, 4095, 8191, 12289, N - 1], dtype=np.int64)
+    xf = oracle.bf16_to_f64(x.x)[0]
+    wqkv = oracle.bf16_to_f64(x.w_qkv)
+    kv = oracle.round_bf16(xf @ wqkv[:, E:])                                  # [N, 2E]
+    q = oracle.round_bf16(xf[rows] @ wqkv[:, :E])                             # [R, E]
+    heads = lambda t, n: np.ascontiguousarray(t.reshape(1, n, H, d).transpose(0, 2, 1, 3))  # noqa: E731
+    k, v = heads(kv[:, :E], N), heads(kv[:, E:], N)
+    # attention_rows wants the query tensor at full length: place the sampled
+    # rows at their positions (other rows are not computed).
+    qf = np.zeros((1, H, N, d))
+    qf[:, :, rows] = heads(q, len(rows))
+    O_ref, lse_ref = oracle.attention_rows(qf, k, v, 1.0 / np.sqrt(d), True, None, rows=rows)
+    attn = oracle.round_bf16(O_ref.transpose(0, 2, 1, 3).reshape(1, len(rows), E))
+    out_ref = attn @ oracle.bf16_to_f64(x.w_o)
+    check(out[:, rows], lse[:, :, rows], out_ref, lse_ref, "long-context block, sampled rows")
