@@ -42,3 +42,54 @@ def test_reused_buffers_hit_and_a_new_pointer_misses():
     assert (h2 - h1, m2 - m1) == (per_call - 1, 1)
     assert sdp.attn_check_device() == sdp.ATTN_OK
     assert torch.equal(first, out)  # same inputs through a freshly encoded map
+
+
+@pytest.mark.gpu
+def test_host_threads_share_the_table():
+    # Four host threads, each with its own buffers and stream, call attn_fwd
+    # concurrently; the table is shared under its lock, evictions included
+    # (more distinct maps than the table holds), and every result matches
+    # the oracle.
+    import threading
+
+    import torch
+
+    import oracle
+    from gpu_util import assert_close, to_dev
+
+    torch.cuda.set_device(0)
+    B, H, N, d = 1, 2, 200, 64
+    scale = 1.0 / np.sqrt(d)
+    inputs = [tuple(I.make_tensor_bits(300 + i, s, (B, H, N, d)) for s in (0, 1, 2)) for i in range(4)]
+    refs = [oracle.attention_rows(q, k, v, scale, True) for q, k, v in inputs]
+    errors = []
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(0)
+            stream = torch.cuda.Stream()
+            q, k, v = (to_dev(t) for t in inputs[i])
+            # 80 output buffers per thread: 320 distinct O maps in all, more
+            # than the table's 256 entries.
+            outs = [torch.empty_like(q) for _ in range(80)]
+            lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+            with torch.cuda.stream(stream):
+                for rep in range(2):
+                    for o in outs:
+                        st = sdp.attn_fwd(q, k, v, o, lse, B, H, N, d, scale, True, None, stream)
+                        assert st == sdp.ATTN_OK, sdp.attn_status_str(st)
+            stream.synchronize()
+            O_ref, lse_ref = refs[i]
+            for o in outs[::16]:
+                O = o.float().cpu().numpy().astype(np.float64)
+                assert_close(O, lse.cpu().numpy().astype(np.float64), O_ref, lse_ref, "thread %d" % i)
+        except Exception as e:  # noqa: BLE001
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(4)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors[0]
+    assert sdp.attn_check_device() == sdp.ATTN_OK
