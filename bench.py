@@ -43,6 +43,9 @@ CSRC = os.path.join(ROOT, "scaled_dot_product_18_b300", "csrc")
 
 
 # Sources each timed kernel is compiled from (its own file plus the shared headers).
+L2_BYTES = 126 * 1000 * 1000   # B300 L2 (126 MB)
+FLUSH_BYTES = 256 << 20        # a write this large evicts every L2 line
+
 KERNEL_SOURCES = {
     "fwd": ("attn_fwd_sm103.cu", "ptx_sm103.cuh", "attn_internal.h"),
     "bwd": ("attn_bwd_sm103.cu", "ptx_sm103.cuh", "attn_internal.h"),
@@ -229,6 +232,59 @@ def capture_steps(step, steps: int):
     return g
 
 
+def timed_device_ms(step, steps: int, stream, sampler, ws: int, flush_l2: bool) -> float:
+    """Device time of `steps` calls of step(), max over ranks, in ms.
+
+    Inputs larger than L2 are timed as one replay of a CUDA graph holding the
+    calls (events around the replay).  Inputs that fit in L2 are timed call by
+    call, each between its own pair of events, with the L2 flushed by a
+    256 MiB write before every call (outside the events; the host queues the
+    call while the write runs), so that no call finds its inputs in L2."""
+    import torch
+    import torch.distributed as dist
+
+    def barrier():
+        if ws > 1:
+            dist.barrier()
+
+    if flush_l2:
+        scratch = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        barrier()
+        torch.cuda.synchronize()
+        with sampler:
+            for i in range(steps):
+                scratch.zero_()
+                starts[i].record(stream)
+                step()
+                ends[i].record(stream)
+            torch.cuda.synchronize()
+        barrier()
+        total = sum(a.elapsed_time(b) for a, b in zip(starts, ends))
+    else:
+        graph = capture_steps(step, steps)  # the timed region replays these calls
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        with sampler:
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+        barrier()
+        total = e0.elapsed_time(e1)
+    return max_over_ranks(total, ws, "cuda")
+
+
+def timing_note(steps: int, flush_l2: bool, what: str) -> dict:
+    if flush_l2:
+        return {"timed": "%d %s calls, each between its own pair of CUDA events" % (steps, what),
+                "l2": "inputs fit in L2: L2 flushed (256 MiB write) before every timed call"}
+    return {"timed": "one CUDA-graph replay of the %d %s calls (after one untimed replay)" % (steps, what),
+            "l2": "inputs larger than L2"}
+
+
 # ----------------------------------------------------------------- main
 
 def max_over_ranks(ms: float, ws: int, device=None) -> float:
@@ -328,18 +384,9 @@ def run_decode(args, w: I.DecodeWorkload, ws: int, rank: int, local: int) -> int
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:  # noqa: BLE001
         uuid = None
-    graph = capture_steps(step, args.steps)  # the timed region replays these calls
     sampler = ClockSampler(uuid)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with sampler:
-        e0.record(stream)
-        graph.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-    ms_step = max_over_ranks(e0.elapsed_time(e1), ws, "cuda") / args.steps
+    flush_l2 = k.numel() * 2 * 2 <= L2_BYTES  # K and V cache bytes
+    ms_step = timed_device_ms(step, args.steps, stream, sampler, ws, flush_l2) / args.steps
     if sdp.attn_check_device(sh) != sdp.ATTN_OK:
         raise RuntimeError("device error in timed steps")
     moved = w.bytes_moved(x.key_lens)
@@ -371,7 +418,7 @@ def run_decode(args, w: I.DecodeWorkload, ws: int, rank: int, local: int) -> int
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d,
-                   "bytes_per_step": moved, "l2": "cache larger than L2" if moved > 126e6 else "fits in L2"},
+                   "bytes_per_step": moved, **timing_note(args.steps, flush_l2, "attn_decode")},
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": gbs / peaks["hbm_gbs"], "traffic": committed_traffic(w.name, "decode"),
                      "peak_source": peaks["source"] + " copy bandwidth (MEASURED_PEAKS.json)",
@@ -424,18 +471,9 @@ def run_mha(args, w: I.MhaWorkload, ws: int, rank: int, local: int) -> int:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:  # noqa: BLE001
         uuid = None
-    graph = capture_steps(step, args.steps)  # the timed region replays these calls
     sampler = ClockSampler(uuid)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with sampler:
-        e0.record(stream)
-        graph.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-    ms_step = max_over_ranks(e0.elapsed_time(e1), ws, "cuda") / args.steps
+    flush_l2 = (tx.numel() + tw.numel() + to.numel()) * 2 <= L2_BYTES
+    ms_step = timed_device_ms(step, args.steps, stream, sampler, ws, flush_l2) / args.steps
     if sdp.attn_check_device(sh) != sdp.ATTN_OK:
         raise RuntimeError("device error in timed steps")
     # end to end: x goes up, the block's output comes back (weights stay resident)
@@ -464,7 +502,7 @@ def run_mha(args, w: I.MhaWorkload, ws: int, rank: int, local: int) -> int:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (random weights)",
         "config": {"workload": w.name, "B": w.B, "N": w.N, "E": w.E, "H": w.H, "causal": w.causal,
-                   "flops_per_step": w.flops()},
+                   "flops_per_step": w.flops(), **timing_note(args.steps, flush_l2, "attn_mha_fwd")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"], "traffic": None,
                      "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
@@ -525,18 +563,9 @@ def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:  # noqa: BLE001
         uuid = None
-    graph = capture_steps(step, args.steps)  # the timed region replays these calls
     sampler = ClockSampler(uuid)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with sampler:
-        e0.record(stream)
-        graph.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-    ms_step = max_over_ranks(e0.elapsed_time(e1), ws, "cuda") / args.steps
+    flush_l2 = 5 * q.numel() * 2 <= L2_BYTES  # q, k, v, O, dO
+    ms_step = timed_device_ms(step, args.steps, stream, sampler, ws, flush_l2) / args.steps
     if sdp.attn_check_device(sh) != sdp.ATTN_OK:
         raise RuntimeError("device error in timed steps")
     # end to end: q, k, v, O, dO and lse go up, dq, dk, dv come back.  As in
@@ -616,7 +645,7 @@ def run_backward(args, w: I.Workload, ws: int, rank: int, local: int) -> int:
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name + "_backward", "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-                   "flops_per_step": flops, "l2": "inputs larger than L2"},
+                   "flops_per_step": flops, **timing_note(args.steps, flush_l2, "attn_bwd")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"],
                      "traffic": committed_traffic(w.name + "_backward", "bwd"),
@@ -719,22 +748,13 @@ def main() -> int:
             dist.barrier()
 
     # ------------------------------------------------ device-resident timing
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     try:
         uuid = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
     except Exception:  # noqa: BLE001 - sample every visible GPU instead
         uuid = None
-    graph = capture_steps(step, args.steps)  # the timed region replays these calls
     sampler = ClockSampler(uuid)
-    barrier()
-    torch.cuda.synchronize()
-    with sampler:
-        e0.record(stream)
-        graph.replay()
-        e1.record(stream)
-        torch.cuda.synchronize()
-    barrier()
-    ms_total = max_over_ranks(e0.elapsed_time(e1), ws, "cuda")
+    flush_l2 = w.algorithmic_bytes() <= L2_BYTES
+    ms_total = timed_device_ms(step, args.steps, stream, sampler, ws, flush_l2)
     st = sdp.attn_check_device(sh)
     if st != sdp.ATTN_OK:
         raise sdp.AttnError(st, "timed steps")
@@ -830,8 +850,7 @@ def main() -> int:
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
                    "key_lens": list(w.key_len_range) if w.key_len_range else None,
                    "flops_per_step": flops, "parallelism": "replica per GPU" if ws > 1 else "single GPU",
-                   "timed": "one CUDA-graph replay of the %d attn_fwd calls (after one untimed replay)" % args.steps,
-                   "l2": "inputs larger than L2" if w.algorithmic_bytes() > 126e6 else "inputs fit in L2 (no flush)"},
+                   **timing_note(args.steps, flush_l2, "attn_fwd")},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
                      "peak_source": peaks["source"] + " bf16 burst (MEASURED_PEAKS.json)",
