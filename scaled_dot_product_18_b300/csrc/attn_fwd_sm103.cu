@@ -22,9 +22,11 @@
 //                  O0 += P0 V_j, S0 = Q0 K_{j+1}^T, O1 += P1 V_j, S1 = ...
 //                so the tensor core works on one tile while the other tile's
 //                warps run the softmax.
-//   warp 9       TMA producer: Q0, Q1 of each work item, then K_j, V_j
-//                through a ring of shared-memory slots guarded by full/empty
-//                mbarriers.
+//   warp 9       TMA producer: works out each work item of the CTA once and
+//                publishes it to the other warps in a small ring of
+//                shared-memory descriptors, then loads Q0, Q1 of the item
+//                and K_j, V_j through a ring of shared-memory slots guarded
+//                by full/empty mbarriers.
 // A softmax warp reads S_t from TMEM, masks the last key tile, takes the
 // running max in the log2 domain, exponentiates with ex2, and writes P_t as
 // packed bf16 back into the first 64 columns of S_t's TMEM region, where the
@@ -32,19 +34,25 @@
 // issue order, so S_t for key tile j+1 (issued after O_t += P_t V_j) only
 // overwrites P_t after that MMA has read it, and the commit that signals
 // "S_t(j+1) ready" also covers O_t += P_t V_j: a softmax warp that holds
-// S_t(j+1) may rescale O_t in place, no MMA is writing it.
+// S_t(j+1) may rescale O_t in place, no MMA is writing it.  At d = 64 the
+// two O tiles leave room for P_t in its own TMEM columns, so S_t(j+1) is
+// issued as soon as the softmax warps have read S_t(j).
 //
-// Work items.  An item is a pair of query tiles of one (batch, head); the
-// grid has min(items, SMs) CTAs and CTA c takes items c, c + grid, c + 2 grid,
-// ... of one fixed order: heaviest causal pair first, within groups of heads
-// whose keys and values stay in L2 (a static version of the hardware's
-// greedy block scheduling, without the per-CTA set-up).  TMEM is allocated,
+// Work items.  An item is a pair of query tiles of one (batch, head).  Work
+// units (an item, or two causal items of equal total cost) run in one fixed
+// order: heaviest causal pair first, within groups of heads whose keys and
+// values stay in L2.  With enough units per SM the grid is min(units, SMs)
+// persistent CTAs and CTA c takes units c, c + grid, ... (a static version
+// of the hardware's greedy block scheduling, without the per-CTA set-up);
+// otherwise each causal item gets its own CTA.  TMEM is allocated,
 // barriers initialised and tensor maps prefetched once per CTA; every
 // barrier keeps counting phases across items.  The softmax warps write O_t
-// straight from registers to global memory, so a Q buffer is free as soon as
-// its last S MMA has run: the next item's Q is loaded while the current
-// item's last key tiles and its epilogue are still in flight, and the
-// tensor core starts the next item while the previous one's O is written.
+// from registers (d = 128) or through a small per-warp staging buffer and a
+// TMA store (d = 64), never through the Q buffers, so a Q buffer is free as
+// soon as its last S MMA has run: the next item's Q is loaded while the
+// current item's last key tiles and its epilogue are still in flight, and
+// the tensor core starts the next item while the previous one's O is
+// written.
 //
 // Q, K and V are addressed through 4-D tensor maps {d, N, H, B} and O through
 // element strides, all with arbitrary row, head and batch strides, so the
@@ -54,7 +62,8 @@
 // Memory layout (all 128-byte swizzled, 1024-byte aligned tiles):
 //   Q tile t : d/64 column blocks of [128 rows x 64 bf16]
 //   K/V ring : NSLOT slots of d/64 blocks of [128 keys x 64 bf16]
-// TMEM (512 columns): S0 at 0, S1 at 128, O0 at 256, O1 at 256 + d.
+// TMEM (512 columns): S0 at 0, S1 at 128, O0 at 256, O1 at 256 + d; at
+// d = 64, P0 at 384 and P1 at 448.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -114,7 +123,9 @@ __device__ __forceinline__ void st_global_v8(void *p, const uint32_t *w)
 // softmax warps read it there instead of repeating the schedule arithmetic
 // (integer divisions, key ranges) at every item boundary.
 constexpr int kDescSlots = 4;
-constexpr int kDescBytes = 48;  // three int4: {q0, b, h, bh}, {kv_len, kr0, kr1.first}, {kr1.end, j_begin, n_max, valid}
+// Three int4: {q0, b, h, bh}, {kv_len, kr0.first, kr0.end, kr1.first},
+// {kr1.end, j_begin, n_max, valid}.
+constexpr int kDescBytes = 48;
 constexpr int kDescConsumers = 1 + 8;  // the MMA warp and the 8 softmax warps (one arrival per warp)
 
 template <int D>
