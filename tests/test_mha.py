@@ -96,3 +96,52 @@ def test_mha_long_context_sampled():
     attn = oracle.round_bf16(O_ref.transpose(0, 2, 1, 3).reshape(1, len(rows), E))
     out_ref = attn @ oracle.bf16_to_f64(x.w_o)
     check(out[:, rows], lse[:, :, rows], out_ref, lse_ref, "long-context block, sampled rows")
+
+
+def test_mha_long_context_projections_elementwise():
+    # Both projection GEMMs of the long-context block at full size, every
+    # element: the workspace holds the bf16 [B*N, 3E] Q/K/V rows (x W_qkv)
+    # and, 256-byte aligned after them, the merged heads M; `out` is M W_o.
+    # Each is compared with the fp64 product of the same bf16 operands.  The
+    # GPU accumulates in fp32 in another order, so where the exact sum lies
+    # within the fp32 error of a bf16 rounding midpoint (about 0.2 % of the
+    # elements at K = 4096), or cancels to far below the terms' size, it may
+    # round differently.
+    import torch
+    w = I.MHA_WORKLOADS["mha_b1n16384e4096h32_causal"]
+    x = I.make_mha_inputs(w)
+    tx, tw, to = to_dev(x.x), to_dev(x.w_qkv), to_dev(x.w_o)
+    out = torch.empty((w.B, w.N, w.E), dtype=torch.bfloat16, device="cuda")
+    nbytes = sdp.attn_mha_workspace_size(w.B, w.N, w.E)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    st = sdp.attn_mha_fwd(tx, tw, to, out, None, w.B, w.N, w.E, w.H, w.causal, None, ws, nbytes,
+                          torch.cuda.current_stream())
+    assert st == sdp.ATTN_OK, sdp.attn_status_str(st)
+    assert sdp.attn_check_device(torch.cuda.current_stream()) == sdp.ATTN_OK
+    rows, E = w.B * w.N, w.E
+    qkv_bytes = (rows * 3 * E * 2 + 255) // 256 * 256
+    qkv = ws[: rows * 3 * E * 2].view(torch.int16).cpu().numpy().view(np.uint16).reshape(rows, 3 * E)
+    merged = ws[qkv_bytes: qkv_bytes + rows * E * 2].view(torch.int16).cpu().numpy().view(np.uint16).reshape(rows, E)
+    got_out = out.view(torch.int16).cpu().numpy().view(np.uint16).reshape(rows, E)
+
+    def check_gemm(a_bits, b_bits, got_bits, what):
+        a, b = oracle.bf16_to_f64(a_bits), oracle.bf16_to_f64(b_bits)
+        exact = a @ b
+        got = oracle.bf16_to_f64(got_bits)
+        # Bound per element: the bf16 rounding of the result (half a step,
+        # 2^-9 relative, doubled for the GPU rounding its own fp32 value) plus
+        # the fp32 accumulation error, which is a few 2^-24 sqrt(K) times the
+        # size of the terms; 2^-18 |a_i| |b_j| (row and column norms, which
+        # bound |sum_k a_ik b_kj| by Cauchy-Schwarz) covers it at K = 4096
+        # while a dropped K step or a misplaced tile is orders larger.
+        tau = 2.0 ** -18 * np.linalg.norm(a, axis=1)[:, None] * np.linalg.norm(b, axis=0)[None, :]
+        err = np.abs(got - exact)
+        bad = err > 2.0 ** -8 * np.abs(exact) + tau
+        assert not bad.any(), "%s: %d elements off, worst %.3e (bound %.3e)" % (
+            what, int(bad.sum()), float(err[bad].max()), float((2.0 ** -8 * np.abs(exact) + tau)[bad].max()))
+        # Most elements are the correctly rounded value itself.
+        frac = float((got != oracle.round_bf16(exact)).mean())
+        assert frac < 1e-2, "%s: %.2e of the elements differ from the rounded exact product" % (what, frac)
+
+    check_gemm(x.x.reshape(rows, E), x.w_qkv, qkv, "x W_qkv")
+    check_gemm(merged, x.w_o, got_out, "M W_o")
